@@ -1,0 +1,184 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: attention over a block-paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow two descriptions of the method:
+ *   [LPNH]   "vLLM推理引擎架构PagedAttention机制与高吞吐推理" (lpnh.cn):
+ *            §2.2 BlockManager (allocate / free over a pool of fixed-size blocks;
+ *            k_cache and v_cache shaped [num_blocks, block_size, num_heads,
+ *            head_dim]); §2.3 PagedAttention Kernel (query, key_cache,
+ *            value_cache, block_tables, context_lens, block_size; look up each
+ *            token's block through block_tables, score inside the block,
+ *            accumulate across blocks; output = empty_like(query)); §4.1 block
+ *            size (default 16).
+ *   [LESSON] "Servis Motor İçleri: PagedAttention, Sürekli Batching, parçalanmış
+ *            Prefill" (aiengineeringfromscratch.com, Phase 17 - 04):
+ *            "PagedAttention as a virtual memory system" (a block table maps
+ *            logical token positions to physical block ids; a sequence gains one
+ *            block when it grows past the ones it holds); "Chunked prefill
+ *            protects the TTFT tail" (512-token prompt chunks scheduled next to
+ *            single-token decodes); "What the scheduler looks like" (one fused GPU
+ *            call per iteration).
+ *
+ * Conventions for every call below
+ *   - Device pointers are CUDA device memory owned by the caller; the library
+ *     never allocates, frees or keeps them.  Host pointers are named host_*.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Kernels are
+ *     launched asynchronously on it; nothing is copied back to the host, so a
+ *     call returns before the GPU has finished.
+ *   - Layouts are row-major and dense:
+ *       q, out                 [tokens, num_heads, head_dim]          bf16
+ *       k, v (new rows)        [num_tokens, num_kv_heads, head_dim]   bf16
+ *       k_cache, v_cache       [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ *       block_tables           [num_seqs, max_blocks_per_seq]         int32
+ *       context_lens           [num_seqs]                             int32
+ *       query_start_loc        [num_seqs + 1], query_start_loc[0] = 0 int32
+ *       slot_mapping           [num_tokens]                           int64
+ *   - Query head h reads KV head h / (num_heads / num_kv_heads).
+ *   - context_lens[s] counts every token of sequence s in the cache, this step's
+ *     new tokens included (write them with pkv_reshape_and_cache first).  A
+ *     sequence's q_len query rows are its last q_len positions.
+ *   - Accumulation is fp32; outputs are rounded to bf16 (round to nearest even).
+ *   - Return value: PKV_OK or a negative PKV_ERR_* code, for argument errors the
+ *     host can see.  Errors in device data (a block id outside the pool, a slot
+ *     outside the pool, a context longer than its block-table row, q_len larger
+ *     than context_len) cannot be seen by the host: the kernels skip the bad
+ *     item, never read or write outside the caller's buffers, and record a flag
+ *     in a device error word that pkv_get_device_error returns.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define PKV_OK                       0
+#define PKV_ERR_INVALID_ARG         -1  /* null pointer, negative or inconsistent size */
+#define PKV_ERR_UNSUPPORTED         -2  /* valid but not built: see each call */
+#define PKV_ERR_WORKSPACE_TOO_SMALL -3  /* workspace_bytes < pkv_workspace_size(...) */
+#define PKV_ERR_CUDA                -4  /* a CUDA runtime call or launch failed */
+#define PKV_ERR_OOM                 -5  /* block manager: not enough free blocks */
+#define PKV_ERR_DEVICE_DATA         -6  /* returned by pkv_get_device_error */
+
+/* ---- flags in the device error word (pkv_get_device_error) ---------------- */
+#define PKV_DEVERR_SLOT         0x1   /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_BLOCK_ID     0x2   /* block_tables entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT_LEN  0x4   /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEVERR_QUERY_LEN    0x8   /* q_len < 0 or q_len > context_len */
+#define PKV_DEVERR_TIMEOUT      0x10  /* a pipeline wait gave up (internal fault) */
+
+/* ---- dtypes --------------------------------------------------------------- */
+#define PKV_DTYPE_BF16 0
+
+/* ---- ops for pkv_workspace_size ------------------------------------------- */
+#define PKV_OP_DECODE 0
+#define PKV_OP_VARLEN 1
+
+/*
+ * KV write ("reshape_and_cache").  [LPNH] §2.2 pool layout; [LESSON] "PagedAttention
+ * as a virtual memory system" (a token's K/V row lives in one slot of a block).
+ * For each token t with slot = slot_mapping[t] >= 0:
+ *     k_cache[slot / block_size][slot % block_size][:][:] = k[t][:][:]   (same for v)
+ * A negative slot marks a padding token and is skipped.  The copy is bit-exact.
+ * Slots >= num_blocks * block_size are skipped and flagged PKV_DEVERR_SLOT.
+ * Two tokens with the same slot race (the result is one of them).
+ * Supported: dtype PKV_DTYPE_BF16, num_kv_heads * head_dim a multiple of 8.
+ */
+int pkv_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
+                          const int64_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                          int block_size, int num_kv_heads, int head_dim, int dtype,
+                          void *stream);
+
+/*
+ * Decode attention: one query row per sequence.  [LPNH] §2.3.
+ * For sequence s and query head h (KV head hk = h / (num_heads / num_kv_heads)):
+ *     out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s
+ * where K_s, V_s are rows 0 .. context_lens[s]-1 of the sequence, row p stored in
+ * block block_tables[s][p / block_size], slot p % block_size.  context_lens[s] = 0
+ * gives a zero row.  Long contexts are split across thread blocks and the parts
+ * merged with their log-sum-exp weights; `workspace` (device, >=
+ * pkv_workspace_size(PKV_OP_DECODE, ...) bytes, 256-byte aligned, contents
+ * irrelevant on entry) holds the parts.  Calls that share a workspace must be
+ * ordered on one stream.
+ * Supported: dtype bf16, block_size 16, head_dim 64 or 128, num_heads a multiple
+ * of num_kv_heads, group = num_heads / num_kv_heads <= 64, num_seqs <= 4096.
+ */
+int pkv_paged_attention_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int max_blocks_per_seq, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               float scale, int dtype, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
+ * Varlen attention over a ragged batch in one call ([LESSON] "Chunked prefill
+ * protects the TTFT tail", "What the scheduler looks like": prefill chunks and
+ * single-token decodes in one fused GPU call).  Sequence s owns query rows
+ * query_start_loc[s] .. query_start_loc[s+1]-1, at positions
+ * context_lens[s] - q_len .. context_lens[s] - 1.  With causal != 0, row j of a
+ * sequence sees keys 0 .. context_lens[s] - q_len + j; otherwise all
+ * context_lens[s] keys.  q_len = 1 rows take the decode path; longer ones the
+ * chunked-prefill path.  total_q_tokens = query_start_loc[num_seqs] and max_q_len
+ * bounds every q_len (both as the caller knows them on the host).
+ * Supported: as for decode, plus total_q_tokens <= 2^31 - 1.
+ */
+int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
+                               const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int total_q_tokens, int max_q_len,
+                               int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, float scale,
+                               int causal, int dtype, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* Workspace bytes the op needs on the current device for these sizes (0 if the
+ * sizes are unsupported).  Does not allocate. */
+size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,
+                          int num_kv_heads, int head_dim, int block_size);
+
+/* Static description of a status code. */
+const char *pkv_status_string(int status);
+
+/* Synchronizes `stream`, then returns and clears the current device's error word
+ * (a bitwise OR of PKV_DEVERR_* flags; 0 = no error).  Negative on a CUDA error. */
+int pkv_get_device_error(void *stream);
+
+/*
+ * Slot mapping on the host (step before the KV write).  [LESSON] "PagedAttention as
+ * a virtual memory system": for new token t of sequence host_token_seq[t] at
+ * absolute position p = host_token_pos[t]:
+ *     host_slot_mapping[t] = host_block_tables[seq][p / block_size] * block_size
+ *                            + p % block_size
+ * host_token_seq[t] < 0 gives -1 (padding).  PKV_ERR_INVALID_ARG if p is negative,
+ * beyond the table row, or lands on a negative table entry.
+ */
+int pkv_slot_mapping(int64_t *host_slot_mapping, const int32_t *host_block_tables,
+                     int max_blocks_per_seq, const int32_t *host_token_seq,
+                     const int32_t *host_token_pos, int64_t num_tokens, int block_size);
+
+/*
+ * Host block manager.  [LPNH] §2.2 BlockManager: a free list over num_blocks
+ * physical block ids; allocate(n) takes the first n free ids or fails with
+ * out-of-memory and changes nothing; free(ids) appends them to the list.  The
+ * handle is host memory owned by the caller (create / destroy).  Not thread-safe.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+pkv_block_manager *pkv_block_manager_create(int64_t num_blocks, int block_size);
+void pkv_block_manager_destroy(pkv_block_manager *bm);
+/* Writes n ids to host_ids_out; PKV_ERR_OOM (nothing taken) if fewer are free. */
+int pkv_block_manager_allocate(pkv_block_manager *bm, int64_t n, int32_t *host_ids_out);
+/* Returns ids to the free list; PKV_ERR_INVALID_ARG (nothing returned) if an id is
+ * outside the pool or not currently allocated. */
+int pkv_block_manager_free(pkv_block_manager *bm, const int32_t *host_ids, int64_t n);
+int64_t pkv_block_manager_num_free(const pkv_block_manager *bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,358 @@
+// api.cu -- the extern "C" entry points of libpagedkv.so (declared in
+// include/pagedkv.h): argument checks, launch planning, TMA descriptors, launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pagedkv.h"
+#include "paged_decode.cuh"
+#include "paged_prefill.cuh"
+
+namespace pkv {
+cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t num_slots, int row_bytes, int num_sms, int *err,
+                                     cudaStream_t stream);
+}
+
+// The device error word (one per device that loads the library).
+__device__ int g_pkv_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kBlockSize = 16;
+constexpr int kMaxDecodeItems = 8192;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    int *err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device facts, looked up once per device with that device current.
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_pkv_device_error) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return PKV_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return PKV_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Tensor map over a KV cache [num_blocks, 16, num_kv_heads, head_dim] seen as
+// [rows = num_blocks * 16][num_kv_heads][head_dim / 64][64]: one box is 16 rows x 64
+// columns (2 KiB) of one head, swizzled 128 bytes.
+int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
+                     int num_kv_heads, int head_dim, int box_rows) {
+    cuuint64_t dims[4] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)num_kv_heads,
+                          (cuuint64_t)(num_blocks * block_size)};
+    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2,
+                             (cuuint64_t)num_kv_heads * head_dim * 2};
+    cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ---- decode planning -------------------------------------------------------
+struct DecodePlan {
+    int group, warps_per_head, heads_per_cta, head_tiles, items, stage_bytes, num_stages, grid;
+    size_t smem;
+    size_t off_prefix, off_ml, off_o, bytes;
+};
+
+int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, const DeviceInfo &d,
+                DecodePlan *p) {
+    p->group = num_heads / num_kv_heads;
+    p->warps_per_head = (p->group + 15) / 16;
+    if (p->warps_per_head > 8) return PKV_ERR_UNSUPPORTED;
+    int ht = 1;
+    for (int c = 1; c <= num_kv_heads; ++c)
+        if (num_kv_heads % c == 0 && c * p->warps_per_head <= 8) ht = c;
+    p->heads_per_cta = ht;
+    p->head_tiles = num_kv_heads / ht;
+    p->items = num_seqs * p->head_tiles;
+    if (p->items > kMaxDecodeItems) return PKV_ERR_UNSUPPORTED;
+    p->stage_bytes = ht * head_dim * kBlockSize * 2;
+    const size_t fixed = pkv::decode_smem_bytes(0, 0, p->items);
+    const int budget = d.smem_optin;
+    int nst = (int)((budget - (int64_t)fixed) / (p->stage_bytes + 16));
+    if (nst > 12) nst = 12;
+    if (nst < 2) return PKV_ERR_UNSUPPORTED;
+    p->num_stages = nst;
+    p->smem = pkv::decode_smem_bytes(p->stage_bytes, nst, p->items);
+    p->grid = d.sms;
+    const size_t rows = (size_t)ht * p->group;
+    p->off_prefix = 0;
+    p->off_ml = round_up(4 * (size_t)(p->items + 1), 256);
+    p->off_o = p->off_ml + round_up(2 * (size_t)p->grid * rows * 8, 256);
+    p->bytes = p->off_o + round_up(2 * (size_t)p->grid * rows * head_dim * 4, 256);
+    return PKV_OK;
+}
+
+int check_common(int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                 int head_dim, int block_size, int64_t num_blocks, int dtype) {
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_blocks * block_size > (int64_t)UINT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * max_blocks_per_seq * num_kv_heads > (int64_t)INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+// Runs the decode kernel on the sequences selected by `query_start_loc` (all if null).
+int run_decode(void *out, const void *q, const int32_t *query_start_loc, int total_q,
+               const void *k_cache,
+               const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+               int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+               int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
+               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream) {
+    if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
+    CUtensorMap kmap, vmap;
+    int st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    if (st == PKV_OK) st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    if (st != PKV_OK) return st;
+    pkv::DecodeArgs a;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start_loc = query_start_loc;
+    a.total_q = total_q;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_heads = num_heads;
+    a.group = p.group;
+    a.heads_per_cta = p.heads_per_cta;
+    a.head_tiles = p.head_tiles;
+    a.warps_per_head = p.warps_per_head;
+    a.num_stages = p.num_stages;
+    a.grid = p.grid;
+    a.min_blocks_per_cta = 8;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.ws_prefix = reinterpret_cast<int32_t *>(ws + p.off_prefix);
+    a.ws_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
+    a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
+    a.err = d.err;
+    return pkv::launch_paged_decode(head_dim, kmap, vmap, a, p.smem, stream) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" const char *pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_OOM: return "out of blocks";
+        case PKV_ERR_DEVICE_DATA: return "invalid device data";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int pkv_get_device_error(void *stream) {
+    DeviceInfo *d = nullptr;
+    int st = device_info(&d);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaMemcpyAsync(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(d->err, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    return h;
+}
+
+extern "C" int pkv_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t num_blocks, int block_size, int num_kv_heads,
+                                     int head_dim, int dtype, void *stream) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
+    if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    int st = device_info(&d);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_reshape_and_cache(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                                                  num_blocks * block_size, (int)row_bytes, d->sms,
+                                                  d->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,
+                                     int num_kv_heads, int head_dim, int block_size) {
+    if (check_common(num_seqs, 0, num_heads, num_kv_heads, head_dim, block_size, 0,
+                     PKV_DTYPE_BF16) != PKV_OK)
+        return 0;
+    DeviceInfo *d = nullptr;
+    if (device_info(&d) != PKV_OK) return 0;
+    DecodePlan p;
+    if (plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p) != PKV_OK) return 0;
+    if (op == PKV_OP_DECODE) return p.bytes;
+    if (op != PKV_OP_VARLEN || total_q_tokens < 0) return 0;
+    pkv::PrefillPlan pp;
+    if (pkv::plan_prefill(num_seqs, num_heads, num_kv_heads, head_dim, d->sms, d->smem_optin,
+                          &pp) != PKV_OK)
+        return round_up(p.bytes, 256);  // decode rows only (prefill rows unsupported)
+    return round_up(p.bytes, 256) + pp.ws_bytes;
+}
+
+extern "C" int pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int64_t num_blocks,
+                                          float scale, int dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, dtype);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    st = device_info(&d);
+    if (st != PKV_OK) return st;
+    DecodePlan p;
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p);
+    if (st != PKV_OK) return st;
+    return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
+                      static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
+                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
+                                          const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int total_q_tokens, int max_q_len,
+                                          int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int64_t num_blocks,
+                                          float scale, int causal, int dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, dtype);
+    if (st != PKV_OK) return st;
+    if (total_q_tokens < 0 || max_q_len < 0) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
+    if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    st = device_info(&d);
+    if (st != PKV_OK) return st;
+    DecodePlan p;
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p);
+    if (st != PKV_OK) return st;
+    pkv::PrefillPlan pp;
+    const bool prefill_rows = max_q_len >= 2;
+    if (prefill_rows) {
+        st = pkv::plan_prefill(num_seqs, num_heads, num_kv_heads, head_dim, d->sms, d->smem_optin,
+                               &pp);
+        if (st != PKV_OK) return st;
+    }
+    const size_t need = round_up(p.bytes, 256) + (prefill_rows ? pp.ws_bytes : 0);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Single-token rows: the decode kernel (it skips every other sequence).
+    st = run_decode(out, q, query_start_loc, total_q_tokens, k_cache, v_cache, block_tables, context_lens,
+                    num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
+                    scale, ws, p.bytes, *d, p, s);
+    if (st != PKV_OK || !prefill_rows) return st;
+    // Multi-token rows (prefill chunks): the chunked-prefill kernel.
+    CUtensorMap kmap, vmap;
+    st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    if (st == PKV_OK) st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    if (st != PKV_OK) return st;
+    pkv::PrefillArgs a;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.query_start_loc = query_start_loc;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.total_q = total_q_tokens;
+    a.num_seqs = num_seqs;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = pp.group;
+    a.tokens_per_tile = pp.tokens_per_tile;
+    a.grid = pp.grid;
+    a.num_stages = pp.num_stages;
+    a.causal = causal != 0;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    uint8_t *pws = ws + round_up(p.bytes, 256);
+    a.ws_seq_prefix = reinterpret_cast<int64_t *>(pws + pp.off_seq_prefix);
+    a.ws_ml = reinterpret_cast<float2 *>(pws + pp.off_ml);
+    a.ws_o = reinterpret_cast<float *>(pws + pp.off_o);
+    a.max_seqs = num_seqs;
+    a.err = d->err;
+    return pkv::launch_paged_prefill(head_dim, kmap, vmap, a, pp, s) == cudaSuccess ? PKV_OK
+                                                                                   : PKV_ERR_CUDA;
+}

@@ -1,0 +1,516 @@
+// paged_decode.cu -- decode attention over a block-paged KV cache (sm_103a), and the
+// log-sum-exp merge of split contexts.
+//
+// Method ("vLLM推理引擎架构PagedAttention机制与高吞吐推理", lpnh.cn, §2.3 PagedAttention
+// Kernel): for each sequence, find each token's KV block through block_tables, score
+// the query against the keys inside the block, and accumulate across blocks.  The
+// accumulation across blocks is an online softmax in fp32 (running max m, running sum
+// l, rescaled output o); parts of one context computed by different thread blocks are
+// merged with their log-sum-exp weights.
+//
+// GB300 design
+//  * Work is the flat list of (sequence, KV-head tile, 16-token block) units.  A
+//    persistent grid of one CTA per SM takes an equal contiguous share of it (+-1
+//    block), so a 32k context and a 500-token one cost the same per block and no SM
+//    idles in a tail.  A CTA's share can start or end inside a sequence: those parts go
+//    to a workspace slot and the merge kernel combines them.
+//  * A CTA covers all KV heads of its tile (8 for Llama-70B shapes), so each pool block
+//    it touches is read as whole 16-token x 2 KiB rows: one producer warp streams K and
+//    V of each block with TMA (128-byte swizzled, evict-first) into a ring of shared
+//    memory stages guarded by mbarriers; the block id comes from the block table.
+//  * One consumer warp per (KV head, 16 query heads): GQA puts the group's query heads
+//    on the 16 rows of an m16n8k16 bf16 tensor-core MMA, so one K/V read from shared
+//    memory serves the whole group.  S = Q K^T and O += P V use ldmatrix fragments from
+//    the swizzled tiles; the S accumulator becomes the P operand without a shuffle.
+//  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
+//    reports PKV_DEVERR_TIMEOUT instead of hanging.
+#include "paged_decode.cuh"
+#include "pkv_split.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBS = 16;  // tokens per block (the fast path's block size)
+
+// Blocks of KV the work item (virtual sequence) v contributes.
+__device__ __forceinline__ int32_t item_blocks(const DecodeArgs &a, int v, bool report) {
+    const int s = v / a.head_tiles;
+    int32_t ctx = a.context_lens[s];
+    if (a.query_start_loc) {
+        const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+        if (q0 < 0 || q1 < q0 || q1 > a.total_q) {
+            if (report) flag_error(a.err, PKV_DEVERR_QUERY_LEN);
+            return 0;
+        }
+        if (q1 - q0 != 1) return 0;  // a prefill chunk (other kernel) or no rows
+        if (ctx < 1) {
+            if (report) flag_error(a.err, PKV_DEVERR_QUERY_LEN);
+            return 0;
+        }
+    }
+    if (ctx < 0 || (int64_t)ctx > (int64_t)a.max_blocks_per_seq * kBS) {
+        if (report) flag_error(a.err, PKV_DEVERR_CONTEXT_LEN);
+        return 0;
+    }
+    return (ctx + kBS - 1) / kBS;
+}
+
+// Exclusive prefix sum of item_blocks over all items, into pre[0..V] (pre[V] = total).
+__device__ void build_prefix(const DecodeArgs &a, int V, int32_t *pre, int32_t *scan_tmp) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (V + nt - 1) / nt;
+    const int beg = min(V, tid * per), end = min(V, beg + per);
+    int32_t local = 0;
+    for (int v = beg; v < end; ++v) local += item_blocks(a, v, blockIdx.x == 0);
+    // inclusive warp scan
+    const int lane = tid & 31, warp = tid >> 5;
+    int32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scan_tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (nt + 31) >> 5;
+        int32_t w = lane < nw ? scan_tmp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) scan_tmp[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    int32_t run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
+    for (int v = beg; v < end; ++v) {
+        pre[v] = run;
+        run += item_blocks(a, v, false);
+    }
+    if (tid == nt - 1) pre[V] = run;
+    __syncthreads();
+}
+
+// Largest v in [0, V) with pre[v] <= f, for 0 <= f < pre[V].
+__device__ __forceinline__ int find_item(const int32_t *pre, int V, int64_t f) {
+    int lo = 0, hi = V;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= f) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(288, 1)
+paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+    constexpr int KSTEPS = D / 16;  // k-steps of the QK^T MMA
+    constexpr int NT_D = D / 8;     // n-tiles of the PV MMA
+    constexpr int DCH = D / 64;     // 64-wide column chunks (one TMA box each)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int HT = a.heads_per_cta;
+    const int NST = a.num_stages;
+    const uint32_t stage_bytes = (uint32_t)HT * D * kBS * 2;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * stage_bytes);
+    uint64_t *empty = full + NST;
+    int32_t *scan_tmp = reinterpret_cast<int32_t *>(empty + NST);  // 32 ints
+    volatile int *abort_flag = scan_tmp + 32;
+    int32_t *pre = scan_tmp + 36;
+
+    const int V = a.num_seqs * a.head_tiles;
+    const int ncw = HT * a.warps_per_head;  // consumer warps
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], ncw);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32 * ncw) {
+        tma_prefetch_desc(&k_map);
+        tma_prefetch_desc(&v_map);
+    }
+    build_prefix(a, V, pre, scan_tmp);  // ends with __syncthreads
+    const int64_t T = pre[V];
+    const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= V; i += blockDim.x) a.ws_prefix[i] = pre[i];
+    }
+    if ((int)blockIdx.x >= ge || T == 0) return;
+    const int c = blockIdx.x;
+    const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
+
+    if (warp == ncw) {
+        // ------------------------------ producer ------------------------------
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued = 0;
+        bool ok = true;
+        for (int64_t f0 = lo; f0 < hi && ok; f0 += 32) {
+            const int64_t f = f0 + lane;
+            int bid = -1, ht = 0;
+            if (f < hi) {
+                const int v = find_item(pre, V, f);
+                const int s = v / a.head_tiles;
+                ht = v - s * a.head_tiles;
+                const int lb = (int)(f - pre[v]);
+                bid = a.block_tables[(int64_t)s * a.max_blocks_per_seq + lb];
+                if (bid < 0 || (int64_t)bid >= a.num_blocks) {
+                    flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    bid = -1;  // TMA fills the out-of-range box with zeros
+                }
+            }
+            const int n = (int)min64(32, hi - f0);
+            for (int j = 0; j < n; ++j) {
+                const int b = __shfl_sync(0xffffffffu, bid, j);
+                const int t = __shfl_sync(0xffffffffu, ht, j);
+                if (lane == 0) {
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                        uint8_t *dst = smem + (size_t)stage * stage_bytes;
+                        const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
+                        for (int dc = 0; dc < DCH; ++dc)
+                            for (int hh = 0; hh < HT; ++hh)
+                                tma_load_4d(dst + (size_t)(dc * HT + hh) * (kBS * 128), map,
+                                            &full[stage], 0, dc, t * HT + hh, b * kBS, policy);
+                        ++issued;
+                        if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+        if (!ok && lane == 0) {
+            flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            // Let the copies already issued land before the CTA's shared memory goes away.
+            const uint32_t pending = minu32(issued, (uint32_t)NST);
+            uint32_t st = stage, ph = phase;
+            for (uint32_t i = 0; i < pending; ++i) {
+                if (st == 0) { st = NST; ph ^= 1; }
+                --st;
+                mbar_wait(&full[st], ph, nullptr);
+            }
+        }
+        return;
+    }
+    if (warp > ncw) return;
+
+    // -------------------------------- consumers --------------------------------
+    const int hh = warp / a.warps_per_head;                 // KV head inside the tile
+    const int r0 = (warp - hh * a.warps_per_head) * 16;     // first query row of the group
+    const int g_row = lane >> 2, q4 = lane & 3;
+    const int group = a.group;
+    const uint32_t smem_base = smem_u32(smem);
+
+    uint32_t stage = 0, phase = 0;
+    int64_t f = lo;
+    while (f < hi) {
+        const int v = find_item(pre, V, f);
+        const int s = v / a.head_tiles;
+        const int ht = v - s * a.head_tiles;
+        const int64_t item_beg = pre[v], item_end = pre[v + 1];
+        const int64_t seg_end = min64(hi, item_end);
+        const int ctx = a.context_lens[s];
+        const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
+        const int kvh = ht * HT + hh;
+        const int rows_valid = min(16, group - r0);  // query heads this warp owns
+
+        // Q fragments (A operand, rows = query heads of the group).
+        uint32_t qa[KSTEPS][4];
+        {
+            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
+                a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D);
+            const bool v0 = g_row < rows_valid, v1 = g_row + 8 < rows_valid;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                const int col = ks * 16 + 2 * q4;
+                qa[ks][0] = v0 ? __ldg(q0 + (g_row * D + col) / 2) : 0u;
+                qa[ks][1] = v1 ? __ldg(q0 + ((g_row + 8) * D + col) / 2) : 0u;
+                qa[ks][2] = v0 ? __ldg(q0 + (g_row * D + col + 8) / 2) : 0u;
+                qa[ks][3] = v1 ? __ldg(q0 + ((g_row + 8) * D + col + 8) / 2) : 0u;
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float o[NT_D][4];
+#pragma unroll
+        for (int n = 0; n < NT_D; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+
+        bool ok = true;
+        for (; f < seg_end; ++f) {
+            const int lb = (int)(f - item_beg);
+            const int valid = min(kBS, ctx - lb * kBS);
+            // ---- S = Q K^T over the block's 16 tokens ----
+            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+            const uint32_t kbase = smem_base + stage * stage_bytes;
+            float sacc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+            {
+                const int mat = lane >> 3, r = lane & 7;
+                const int tok = ((mat >> 1) << 3) + r;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const int col = ks * 16 + ((mat & 1) << 3);
+                    const uint32_t addr = kbase + ((col >> 6) * HT + hh) * (kBS * 128) + swz128(tok, col & 63);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(addr, b0, b1, b2, b3);
+                    mma_bf16_16816(sacc[0], qa[ks], b0, b1);
+                    mma_bf16_16816(sacc[1], qa[ks], b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == (uint32_t)a.num_stages) { stage = 0; phase ^= 1; }
+
+            // ---- online softmax (base 2) ----
+            float mx0 = m0, mx1 = m1;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = nt * 8 + 2 * q4 + e;
+                    const bool in = tok < valid;
+                    sacc[nt][e] = in ? sacc[nt][e] * a.scale_log2 : -INFINITY;
+                    sacc[nt][2 + e] = in ? sacc[nt][2 + e] * a.scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, sacc[nt][e]);
+                    mx1 = fmaxf(mx1, sacc[nt][2 + e]);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float alpha0 = fast_exp2(m0 - mx0), alpha1 = fast_exp2(m1 - mx1);
+            m0 = mx0;
+            m1 = mx1;
+            uint32_t pa[4];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t p01 = pack_bf16x2(fast_exp2(sacc[nt][0] - mx0), fast_exp2(sacc[nt][1] - mx0));
+                const uint32_t p23 = pack_bf16x2(fast_exp2(sacc[nt][2] - mx1), fast_exp2(sacc[nt][3] - mx1));
+                ps0 += bf16_lo(p01) + bf16_hi(p01);
+                ps1 += bf16_lo(p23) + bf16_hi(p23);
+                pa[nt * 2 + 0] = p01;
+                pa[nt * 2 + 1] = p23;
+            }
+            l0 = l0 * alpha0 + ps0;
+            l1 = l1 * alpha1 + ps1;
+#pragma unroll
+            for (int n = 0; n < NT_D; ++n) {
+                o[n][0] *= alpha0;
+                o[n][1] *= alpha0;
+                o[n][2] *= alpha1;
+                o[n][3] *= alpha1;
+            }
+
+            // ---- O += P V ----
+            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+            const uint32_t vbase = smem_base + stage * stage_bytes;
+            {
+                const int mat = lane >> 3, r = lane & 7;
+                const int tok = ((mat & 1) << 3) + r;
+                // Rows past the context hold whatever the pool held (possibly NaN):
+                // zero them in the fragments, since 0 * NaN would poison the sum.
+                const uint32_t keep_lo0 = (2 * q4 < valid ? 0x0000ffffu : 0u) |
+                                          (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
+                const uint32_t keep_hi0 = (8 + 2 * q4 < valid ? 0x0000ffffu : 0u) |
+                                          (8 + 2 * q4 + 1 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int n2 = 0; n2 < NT_D / 2; ++n2) {
+                    const int col = n2 * 16 + ((mat >> 1) << 3);
+                    const uint32_t addr = vbase + ((col >> 6) * HT + hh) * (kBS * 128) + swz128(tok, col & 63);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                    b0 &= keep_lo0;
+                    b1 &= keep_hi0;
+                    b2 &= keep_lo0;
+                    b3 &= keep_hi0;
+                    mma_bf16_16816(o[2 * n2], pa, b0, b1);
+                    mma_bf16_16816(o[2 * n2 + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == (uint32_t)a.num_stages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            return;
+        }
+
+        // ---- finish this item's part ----
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const int64_t seg_beg = max64(lo, item_beg);
+        const bool whole = seg_beg == item_beg && seg_end == item_end;
+        if (whole) {
+            const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
+#pragma unroll
+            for (int n = 0; n < NT_D; ++n) {
+                const int col = n * 8 + 2 * q4;
+                if (g_row < rows_valid)
+                    *reinterpret_cast<uint32_t *>(orow + g_row * D + col) =
+                        pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+                if (g_row + 8 < rows_valid)
+                    *reinterpret_cast<uint32_t *>(orow + (g_row + 8) * D + col) =
+                        pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+            }
+        } else {
+            const int ge_local = split_ctas(T, a.grid, a.min_blocks_per_cta);
+            const int slot = part_slot(c, item_beg, T, ge_local);
+            const int rows = HT * group;
+            const int row0 = hh * group + r0;  // row inside the item
+            float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D;
+            float2 *mlb = a.ws_ml + (int64_t)slot * rows + row0;
+#pragma unroll
+            for (int n = 0; n < NT_D; ++n) {
+                const int col = n * 8 + 2 * q4;
+                if (g_row < rows_valid)
+                    *reinterpret_cast<float2 *>(ob + g_row * D + col) = make_float2(o[n][0], o[n][1]);
+                if (g_row + 8 < rows_valid)
+                    *reinterpret_cast<float2 *>(ob + (g_row + 8) * D + col) = make_float2(o[n][2], o[n][3]);
+            }
+            if (q4 == 0) {
+                if (g_row < rows_valid) mlb[g_row] = make_float2(m0, l0);
+                if (g_row + 8 < rows_valid) mlb[g_row + 8] = make_float2(m1, l1);
+            }
+        }
+        f = seg_end;
+    }
+}
+
+// Merge kernel: one CTA per boundary between neighbouring CTA shares.  It combines
+// the parts of the item split at that boundary (if the boundary is that item's first
+// split) as o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with M = max_p m_p, and
+// writes zero rows for decode rows whose context is empty.
+template <int D>
+__global__ void __launch_bounds__(256)
+paged_decode_merge_kernel(const DecodeArgs a) {
+    const int V = a.num_seqs * a.head_tiles;
+    const int32_t *pre = a.ws_prefix;
+    const int64_t T = pre[V];
+    const int rows = a.heads_per_cta * a.group;
+
+    // Zero rows of empty decode items.
+    for (int v = blockIdx.x; v < V; v += gridDim.x) {
+        if (pre[v] != pre[v + 1]) continue;
+        const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
+        int64_t qrow = s;
+        if (a.query_start_loc) {
+            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+            if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
+            qrow = q0;
+        }
+        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
+        for (int i = threadIdx.x; i < rows * D / 2; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(orow)[i] = 0u;
+    }
+    if (T == 0) return;
+    const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
+    const int b = blockIdx.x;
+    if (b >= ge - 1) return;
+    const int64_t f = share_begin(b + 1, T, ge);  // first block of CTA b+1
+    // item containing f
+    int lo = 0, hi = V;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= f) lo = mid; else hi = mid;
+    }
+    const int v = lo;
+    const int64_t item_beg = pre[v], item_end = pre[v + 1];
+    if (item_beg == f) return;                          // boundary between items
+    if (item_beg < share_begin(b, T, ge)) return;       // split earlier: merged elsewhere
+    const int c0 = b, c1 = share_owner(item_end - 1, T, ge);
+    const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
+    const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
+    __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
+    constexpr int D4 = D / 4;
+    for (int task = threadIdx.x; task < rows * D4; task += blockDim.x) {
+        const int row = task / D4, d4 = task - row * D4;
+        float M = -INFINITY;
+        for (int cc = c0; cc <= c1; ++cc) {
+            const int slot = part_slot(cc, item_beg, T, ge);
+            M = fmaxf(M, a.ws_ml[(int64_t)slot * rows + row].x);
+        }
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cc = c0; cc <= c1; ++cc) {
+            const int slot = part_slot(cc, item_beg, T, ge);
+            const float2 ml = a.ws_ml[(int64_t)slot * rows + row];
+            const float w = fast_exp2(ml.x - M);
+            L += w * ml.y;
+            const float4 ov = reinterpret_cast<const float4 *>(a.ws_o + ((int64_t)slot * rows + row) * D)[d4];
+            acc.x += w * ov.x;
+            acc.y += w * ov.y;
+            acc.z += w * ov.z;
+            acc.w += w * ov.w;
+        }
+        const float inv = 1.f / L;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        reinterpret_cast<uint2 *>(orow + (int64_t)row * D)[d4] = packed;
+    }
+}
+
+template __global__ void paged_decode_kernel<64>(const __grid_constant__ CUtensorMap,
+                                                 const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<128>(const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_merge_kernel<64>(const DecodeArgs);
+template __global__ void paged_decode_merge_kernel<128>(const DecodeArgs);
+
+// ---- host-side launch ----------------------------------------------------------
+
+size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items) {
+    return 1024 + (size_t)num_stages * stage_bytes + 2 * 8 * (size_t)num_stages + 36 * 4 +
+           4 * (size_t)(num_items + 1);
+}
+
+cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                const DecodeArgs &a, size_t smem, cudaStream_t stream) {
+    const int ncw = a.heads_per_cta * a.warps_per_head;
+    const dim3 block((ncw + 1) * 32);
+    cudaError_t e;
+    if (head_dim == 128) {
+        e = cudaFuncSetAttribute(paged_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<128><<<a.grid, block, smem, stream>>>(k_map, v_map, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        paged_decode_merge_kernel<128><<<a.grid, 256, 0, stream>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(paged_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<64><<<a.grid, block, smem, stream>>>(k_map, v_map, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        paged_decode_merge_kernel<64><<<a.grid, 256, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,40 @@
+// paged_decode.cuh -- arguments and launcher of the decode kernel (paged_decode.cu).
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// Everything the decode kernel and its merge kernel read.  A work item ("virtual
+// sequence") is one (sequence, tile of heads_per_cta KV heads); item v = s *
+// head_tiles + tile.
+struct DecodeArgs {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start_loc;  // null: decode (row s); else only q_len == 1 sequences
+    int total_q;                     // rows of q and out
+    int num_seqs;
+    int max_blocks_per_seq;
+    int num_heads;
+    int group;           // num_heads / num_kv_heads
+    int heads_per_cta;   // KV heads per work item
+    int head_tiles;      // num_kv_heads / heads_per_cta
+    int warps_per_head;  // ceil(group / 16)
+    int num_stages;      // shared-memory ring depth (K and V of a block take one stage each)
+    int grid;            // CTAs launched
+    int min_blocks_per_cta;
+    int64_t num_blocks;
+    float scale_log2;    // scale * log2(e)
+    int32_t *ws_prefix;  // [items + 1]
+    float2 *ws_ml;       // [2 * grid][heads_per_cta * group]  (running max, sum)
+    float *ws_o;         // [2 * grid][heads_per_cta * group][head_dim]
+    int *err;            // device error word
+};
+
+size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items);
+cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                const DecodeArgs &a, size_t smem, cudaStream_t stream);
+
+}  // namespace pkv

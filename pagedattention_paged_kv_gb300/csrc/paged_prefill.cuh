@@ -1,0 +1,50 @@
+// paged_prefill.cuh -- arguments, plan and launcher of the chunked-prefill kernel
+// (paged_prefill.cu): attention for every sequence of a varlen batch with q_len >= 2.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// A work item ("tile") is tokens_per_tile consecutive query tokens of one sequence
+// together with all `group` query heads of one KV head: rows r = token * group + head,
+// at most 16 * max_warps rows.  Its units are the 16-token key blocks it must visit.
+struct PrefillArgs {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const int32_t *query_start_loc;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int total_q;  // rows of q and out
+    int num_seqs;
+    int max_blocks_per_seq;
+    int num_heads;
+    int num_kv_heads;
+    int group;
+    int tokens_per_tile;  // a multiple of 16
+    int grid;
+    int num_stages;
+    bool causal;
+    int64_t num_blocks;
+    float scale_log2;
+    int64_t *ws_seq_prefix;  // [num_seqs + 1] units before each sequence
+    float2 *ws_ml;           // [2 * grid][rows]
+    float *ws_o;             // [2 * grid][rows][head_dim]
+    int max_seqs;
+    int *err;
+};
+
+struct PrefillPlan {
+    int group, tokens_per_tile, rows, warps, grid, num_stages, stage_bytes, max_seqs;
+    size_t smem;
+    size_t off_seq_prefix, off_ml, off_o, ws_bytes;
+};
+
+// Fills *p for these sizes (num_seqs bounds the per-sequence table); PKV_OK or
+// PKV_ERR_UNSUPPORTED.
+int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
+                 int smem_optin, PrefillPlan *p);
+cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                 const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream);
+
+}  // namespace pkv

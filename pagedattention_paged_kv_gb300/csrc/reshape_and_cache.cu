@@ -1,0 +1,55 @@
+// reshape_and_cache.cu -- the KV write (sm_103a).
+//
+// "vLLM推理引擎架构PagedAttention机制与高吞吐推理" (lpnh.cn) §2.2: the pool is
+// [num_blocks, block_size, num_kv_heads, head_dim] for K and for V, so slot
+// (block * block_size + offset) of the pool starts num_kv_heads * head_dim elements
+// times the slot into the array.  Each new token's K row and V row are copied there
+// unchanged (bit-exact).
+//
+// One warp per (token, K-or-V) row: the row (num_kv_heads * head_dim * 2 bytes,
+// 2 KiB for Llama-70B shapes) moves as 16-byte vectors, fully coalesced on both sides.
+// The source is read once (no L1 allocation); the destination is written normally.
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+__global__ void __launch_bounds__(256)
+reshape_and_cache_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                         const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                         int64_t num_slots, int row_vecs, int *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         w < 2 * num_tokens; w += warps) {
+        const int64_t t = w >> 1;
+        const bool is_v = (w & 1) != 0;
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;  // padding token
+        if (slot >= num_slots) {
+            if (lane == 0 && !is_v) flag_error(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const uint4 *src = (is_v ? v : k) + t * row_vecs;
+        uint4 *dst = (is_v ? v_cache : k_cache) + slot * row_vecs;
+        for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldcs(src + i);
+    }
+}
+
+cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t num_slots, int row_bytes, int num_sms, int *err,
+                                     cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int warps_per_cta = 8;
+    int64_t ctas = (2 * num_tokens + warps_per_cta - 1) / warps_per_cta;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (ctas > cap) ctas = cap;
+    reshape_and_cache_kernel<<<(unsigned)ctas, warps_per_cta * 32, 0, stream>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        num_slots, row_bytes / 16, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv
