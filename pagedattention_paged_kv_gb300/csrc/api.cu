@@ -76,18 +76,22 @@ int device_info(DeviceInfo **out) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tensor map over a KV cache [num_blocks, 16, num_kv_heads, head_dim] seen as
-// [rows = num_blocks * 16][num_kv_heads][head_dim / 64][64]: one box is 16 rows x 64
-// columns (2 KiB) of one head, swizzled 128 bytes.
+// Tensor map over a KV cache [num_blocks][16][num_kv_heads][head_dim] with its
+// dimensions listed as (column in a 64-wide chunk, token, head, chunk, block): the
+// strides are not in memory order, which lets one box of 16 tokens x box_heads heads x
+// 64 columns land in shared memory as [head][token][64] -- every head's 16 rows
+// contiguous, so the 128-byte swizzle spreads an 8-token ldmatrix over all banks.  One
+// box moves box_heads * 2 KiB; a block's K (or V) for box_heads heads takes
+// head_dim / 64 boxes.
 int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
-                     int num_kv_heads, int head_dim, int box_rows) {
-    cuuint64_t dims[4] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)num_kv_heads,
-                          (cuuint64_t)(num_blocks * block_size)};
-    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2,
-                             (cuuint64_t)num_kv_heads * head_dim * 2};
-    cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_rows};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+                     int num_kv_heads, int head_dim, int box_heads) {
+    const cuuint64_t row = (cuuint64_t)num_kv_heads * head_dim * 2;  // bytes per token
+    cuuint64_t dims[5] = {64, (cuuint64_t)block_size, (cuuint64_t)num_kv_heads,
+                          (cuuint64_t)(head_dim / 64), (cuuint64_t)num_blocks};
+    cuuint64_t strides[4] = {row, (cuuint64_t)head_dim * 2, 128, row * block_size};
+    cuuint32_t box[5] = {64, (cuuint32_t)block_size, (cuuint32_t)box_heads, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -121,7 +125,7 @@ int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, con
     if (nst < 2) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
     p->smem = pkv::decode_smem_bytes(p->stage_bytes, nst, p->items);
-    p->grid = d.sms;
+    p->grid = d.sms < 256 ? d.sms : 256;  // the merge kernels hold <= 256 parts per item
     const size_t rows = (size_t)ht * p->group;
     p->off_prefix = 0;
     p->off_ml = round_up(4 * (size_t)(p->items + 1), 256);
@@ -155,8 +159,11 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
     CUtensorMap kmap, vmap;
-    int st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
-    if (st == PKV_OK) st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    int st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
+                              p.heads_per_cta);
+    if (st == PKV_OK)
+        st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
+                              p.heads_per_cta);
     if (st != PKV_OK) return st;
     pkv::DecodeArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -326,8 +333,9 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     if (st != PKV_OK || !prefill_rows) return st;
     // Multi-token rows (prefill chunks): the chunked-prefill kernel.
     CUtensorMap kmap, vmap;
-    st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
-    if (st == PKV_OK) st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, kBlockSize);
+    st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
+    if (st == PKV_OK)
+        st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
     if (st != PKV_OK) return st;
     pkv::PrefillArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);

@@ -24,6 +24,7 @@
 //    the swizzled tiles; the S accumulator becomes the P operand without a shuffle.
 //  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
 //    reports PKV_DEVERR_TIMEOUT instead of hanging.
+#include "attn_block.cuh"
 #include "paged_decode.cuh"
 #include "pkv_split.cuh"
 
@@ -119,6 +120,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     const int HT = a.heads_per_cta;
     const int NST = a.num_stages;
     const uint32_t stage_bytes = (uint32_t)HT * D * kBS * 2;
+    const uint32_t chunk_stride = (uint32_t)HT * kBS * 128;  // between 64-column sub-tiles
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * stage_bytes);
     uint64_t *empty = full + NST;
     int32_t *scan_tmp = reinterpret_cast<int32_t *>(empty + NST);  // 32 ints
@@ -141,6 +143,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         tma_prefetch_desc(&k_map);
         tma_prefetch_desc(&v_map);
     }
+    // Everything above overlaps the previous kernel; from here on we read its output.
+    pdl_wait();
+    pdl_trigger();
     build_prefix(a, V, pre, scan_tmp);  // ends with __syncthreads
     const int64_t T = pre[V];
     const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
@@ -185,10 +190,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                         mbar_arrive_expect_tx(&full[stage], stage_bytes);
                         uint8_t *dst = smem + (size_t)stage * stage_bytes;
                         const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
+#pragma unroll
                         for (int dc = 0; dc < DCH; ++dc)
-                            for (int hh = 0; hh < HT; ++hh)
-                                tma_load_4d(dst + (size_t)(dc * HT + hh) * (kBS * 128), map,
-                                            &full[stage], 0, dc, t * HT + hh, b * kBS, policy);
+                            tma_load_5d(dst + dc * chunk_stride, map, &full[stage], 0, 0, t * HT,
+                                        dc, b, policy);
                         ++issued;
                         if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
                     }
@@ -219,9 +224,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     const int g_row = lane >> 2, q4 = lane & 3;
     const int group = a.group;
     const uint32_t smem_base = smem_u32(smem);
+    const float sl2 = a.scale_log2;
 
     uint32_t stage = 0, phase = 0;
     int64_t f = lo;
+    RowState<D> st;
     while (f < hi) {
         const int v = find_item(pre, V, f);
         const int s = v / a.head_tiles;
@@ -248,10 +255,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                 qa[ks][3] = v1 ? __ldg(q0 + ((g_row + 8) * D + col + 8) / 2) : 0u;
             }
         }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float o[NT_D][4];
-#pragma unroll
-        for (int n = 0; n < NT_D; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        st.reset();
 
         bool ok = true;
         for (; f < seg_end; ++f) {
@@ -259,98 +263,41 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             const int valid = min(kBS, ctx - lb * kBS);
             // ---- S = Q K^T over the block's 16 tokens ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            const uint32_t kbase = smem_base + stage * stage_bytes;
             float sacc[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-            {
-                const int mat = lane >> 3, r = lane & 7;
-                const int tok = ((mat >> 1) << 3) + r;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    const int col = ks * 16 + ((mat & 1) << 3);
-                    const uint32_t addr = kbase + ((col >> 6) * HT + hh) * (kBS * 128) + swz128(tok, col & 63);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(sacc[0], qa[ks], b0, b1);
-                    mma_bf16_16816(sacc[1], qa[ks], b2, b3);
-                }
-            }
+            qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)a.num_stages) { stage = 0; phase ^= 1; }
+            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
 
-            // ---- online softmax (base 2) ----
-            float mx0 = m0, mx1 = m1;
+            // ---- scale, mask the block's tail, online softmax (base 2) ----
+            const bool tail = valid < kBS;  // only a sequence's last block
+            if (tail) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = nt * 8 + 2 * q4 + e;
-                    const bool in = tok < valid;
-                    sacc[nt][e] = in ? sacc[nt][e] * a.scale_log2 : -INFINITY;
-                    sacc[nt][2 + e] = in ? sacc[nt][2 + e] * a.scale_log2 : -INFINITY;
-                    mx0 = fmaxf(mx0, sacc[nt][e]);
-                    mx1 = fmaxf(mx1, sacc[nt][2 + e]);
+                    for (int e = 0; e < 2; ++e) {
+                        const bool in = nt * 8 + 2 * q4 + e < valid;
+                        sacc[nt][e] = in ? sacc[nt][e] * sl2 : -INFINITY;
+                        sacc[nt][2 + e] = in ? sacc[nt][2 + e] * sl2 : -INFINITY;
+                    }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sacc[0][i] *= sl2;
+                    sacc[1][i] *= sl2;
                 }
             }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float alpha0 = fast_exp2(m0 - mx0), alpha1 = fast_exp2(m1 - mx1);
-            m0 = mx0;
-            m1 = mx1;
             uint32_t pa[4];
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t p01 = pack_bf16x2(fast_exp2(sacc[nt][0] - mx0), fast_exp2(sacc[nt][1] - mx0));
-                const uint32_t p23 = pack_bf16x2(fast_exp2(sacc[nt][2] - mx1), fast_exp2(sacc[nt][3] - mx1));
-                ps0 += bf16_lo(p01) + bf16_hi(p01);
-                ps1 += bf16_lo(p23) + bf16_hi(p23);
-                pa[nt * 2 + 0] = p01;
-                pa[nt * 2 + 1] = p23;
-            }
-            l0 = l0 * alpha0 + ps0;
-            l1 = l1 * alpha1 + ps1;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                o[n][0] *= alpha0;
-                o[n][1] *= alpha0;
-                o[n][2] *= alpha1;
-                o[n][3] *= alpha1;
-            }
+            softmax_update<D>(st, sacc, pa);
 
             // ---- O += P V ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            const uint32_t vbase = smem_base + stage * stage_bytes;
-            {
-                const int mat = lane >> 3, r = lane & 7;
-                const int tok = ((mat & 1) << 3) + r;
-                // Rows past the context hold whatever the pool held (possibly NaN):
-                // zero them in the fragments, since 0 * NaN would poison the sum.
-                const uint32_t keep_lo0 = (2 * q4 < valid ? 0x0000ffffu : 0u) |
-                                          (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-                const uint32_t keep_hi0 = (8 + 2 * q4 < valid ? 0x0000ffffu : 0u) |
-                                          (8 + 2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int n2 = 0; n2 < NT_D / 2; ++n2) {
-                    const int col = n2 * 16 + ((mat >> 1) << 3);
-                    const uint32_t addr = vbase + ((col >> 6) * HT + hh) * (kBS * 128) + swz128(tok, col & 63);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                    b0 &= keep_lo0;
-                    b1 &= keep_hi0;
-                    b2 &= keep_lo0;
-                    b3 &= keep_hi0;
-                    mma_bf16_16816(o[2 * n2], pa, b0, b1);
-                    mma_bf16_16816(o[2 * n2 + 1], pa, b2, b3);
-                }
-            }
+            const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
+            if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
+            else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)a.num_stages) { stage = 0; phase ^= 1; }
+            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
         }
         if (!ok) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -359,28 +306,24 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         }
 
         // ---- finish this item's part ----
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        finish_sums<D>(st);
         const int64_t seg_beg = max64(lo, item_beg);
         const bool whole = seg_beg == item_beg && seg_end == item_end;
         if (whole) {
-            const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+            const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
             __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
 #pragma unroll
             for (int n = 0; n < NT_D; ++n) {
                 const int col = n * 8 + 2 * q4;
                 if (g_row < rows_valid)
                     *reinterpret_cast<uint32_t *>(orow + g_row * D + col) =
-                        pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+                        pack_bf16x2(st.o[n][0] * inv0, st.o[n][1] * inv0);
                 if (g_row + 8 < rows_valid)
                     *reinterpret_cast<uint32_t *>(orow + (g_row + 8) * D + col) =
-                        pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+                        pack_bf16x2(st.o[n][2] * inv1, st.o[n][3] * inv1);
             }
         } else {
-            const int ge_local = split_ctas(T, a.grid, a.min_blocks_per_cta);
-            const int slot = part_slot(c, item_beg, T, ge_local);
+            const int slot = part_slot(c, item_beg, T, ge);
             const int rows = HT * group;
             const int row0 = hh * group + r0;  // row inside the item
             float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D;
@@ -389,51 +332,59 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             for (int n = 0; n < NT_D; ++n) {
                 const int col = n * 8 + 2 * q4;
                 if (g_row < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + g_row * D + col) = make_float2(o[n][0], o[n][1]);
+                    *reinterpret_cast<float2 *>(ob + g_row * D + col) = make_float2(st.o[n][0], st.o[n][1]);
                 if (g_row + 8 < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + (g_row + 8) * D + col) = make_float2(o[n][2], o[n][3]);
+                    *reinterpret_cast<float2 *>(ob + (g_row + 8) * D + col) = make_float2(st.o[n][2], st.o[n][3]);
             }
             if (q4 == 0) {
-                if (g_row < rows_valid) mlb[g_row] = make_float2(m0, l0);
-                if (g_row + 8 < rows_valid) mlb[g_row + 8] = make_float2(m1, l1);
+                if (g_row < rows_valid) mlb[g_row] = make_float2(st.m0, st.l0);
+                if (g_row + 8 < rows_valid) mlb[g_row + 8] = make_float2(st.m1, st.l1);
             }
         }
         f = seg_end;
     }
 }
 
-// Merge kernel: one CTA per boundary between neighbouring CTA shares.  It combines
-// the parts of the item split at that boundary (if the boundary is that item's first
-// split) as o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with M = max_p m_p, and
-// writes zero rows for decode rows whose context is empty.
+// Merge kernel, grid (grid, kMergeRowSplit): CTA (b, y) handles rows y, y + Y, ... of
+// the item split at the boundary between CTA shares b and b+1, if that boundary is the
+// item's first split.  Parts p (one per CTA share that touched the item) combine as
+//     o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,   M = max_p m_p.
+// The CTAs with y == 0 also write zero rows for decode rows whose context is empty.
+constexpr int kMergeRowSplit = 4;
+constexpr int kMergeMaxRows = 32;    // rows per CTA (ceil(rows / kMergeRowSplit) <= 32)
+constexpr int kMergeSmemParts = 16;  // weights of the first parts kept in shared memory
+
 template <int D>
 __global__ void __launch_bounds__(256)
 paged_decode_merge_kernel(const DecodeArgs a) {
+    __shared__ float s_w[kMergeMaxRows][kMergeSmemParts];
+    __shared__ float s_base[kMergeMaxRows], s_inv[kMergeMaxRows];
+    pdl_wait();
     const int V = a.num_seqs * a.head_tiles;
     const int32_t *pre = a.ws_prefix;
     const int64_t T = pre[V];
     const int rows = a.heads_per_cta * a.group;
 
-    // Zero rows of empty decode items.
-    for (int v = blockIdx.x; v < V; v += gridDim.x) {
-        if (pre[v] != pre[v + 1]) continue;
-        const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
-        int64_t qrow = s;
-        if (a.query_start_loc) {
-            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-            if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
-            qrow = q0;
+    if (blockIdx.y == 0) {
+        for (int v = blockIdx.x; v < V; v += gridDim.x) {
+            if (pre[v] != pre[v + 1]) continue;
+            const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
+            int64_t qrow = s;
+            if (a.query_start_loc) {
+                const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+                if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
+                qrow = q0;
+            }
+            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
+            for (int i = threadIdx.x; i < rows * D / 2; i += blockDim.x)
+                reinterpret_cast<uint32_t *>(orow)[i] = 0u;
         }
-        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
-        for (int i = threadIdx.x; i < rows * D / 2; i += blockDim.x)
-            reinterpret_cast<uint32_t *>(orow)[i] = 0u;
     }
     if (T == 0) return;
     const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
     const int b = blockIdx.x;
     if (b >= ge - 1) return;
     const int64_t f = share_begin(b + 1, T, ge);  // first block of CTA b+1
-    // item containing f
     int lo = 0, hi = V;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -444,35 +395,54 @@ paged_decode_merge_kernel(const DecodeArgs a) {
     if (item_beg == f) return;                          // boundary between items
     if (item_beg < share_begin(b, T, ge)) return;       // split earlier: merged elsewhere
     const int c0 = b, c1 = share_owner(item_end - 1, T, ge);
+    const int nparts = c1 - c0 + 1;
     const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
     const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
-    __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
-    constexpr int D4 = D / 4;
-    for (int task = threadIdx.x; task < rows * D4; task += blockDim.x) {
-        const int row = task / D4, d4 = task - row * D4;
+    __nv_bfloat16 *orow0 = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
+
+    // my rows: r = blockIdx.y + k * kMergeRowSplit
+    const int my_rows = (rows - (int)blockIdx.y + kMergeRowSplit - 1) / kMergeRowSplit;
+    // 1) per row: weights w_p = 2^(m_p - M) / sum_q 2^(m_q - M) l_q
+    for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
+        const int row = blockIdx.y + k * kMergeRowSplit;
         float M = -INFINITY;
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int slot = part_slot(cc, item_beg, T, ge);
-            M = fmaxf(M, a.ws_ml[(int64_t)slot * rows + row].x);
-        }
+        for (int p = 0; p < nparts; ++p)
+            M = fmaxf(M, a.ws_ml[(int64_t)part_slot(c0 + p, item_beg, T, ge) * rows + row].x);
         float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int slot = part_slot(cc, item_beg, T, ge);
-            const float2 ml = a.ws_ml[(int64_t)slot * rows + row];
+        for (int p = 0; p < nparts; ++p) {
+            const float2 ml = a.ws_ml[(int64_t)part_slot(c0 + p, item_beg, T, ge) * rows + row];
             const float w = fast_exp2(ml.x - M);
             L += w * ml.y;
+            if (p < kMergeSmemParts) s_w[k][p] = w;
+        }
+        const float inv = 1.f / L;
+        for (int p = 0; p < nparts && p < kMergeSmemParts; ++p) s_w[k][p] *= inv;
+        s_base[k] = M;
+        s_inv[k] = inv;
+    }
+    __syncthreads();
+    // 2) weighted sums, 4 columns per task
+    constexpr int D4 = D / 4;
+    for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
+        const int k = task / D4, d4 = task - k * D4;
+        const int row = blockIdx.y + k * kMergeRowSplit;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int p = 0; p < nparts; ++p) {
+            const int slot = part_slot(c0 + p, item_beg, T, ge);
+            const float w = p < kMergeSmemParts
+                                ? s_w[k][p]
+                                : fast_exp2(a.ws_ml[(int64_t)slot * rows + row].x - s_base[k]) * s_inv[k];
             const float4 ov = reinterpret_cast<const float4 *>(a.ws_o + ((int64_t)slot * rows + row) * D)[d4];
             acc.x += w * ov.x;
             acc.y += w * ov.y;
             acc.z += w * ov.z;
             acc.w += w * ov.w;
         }
-        const float inv = 1.f / L;
         uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        reinterpret_cast<uint2 *>(orow + (int64_t)row * D)[d4] = packed;
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2 *>(orow0 + (int64_t)row * D)[d4] = packed;
     }
 }
 
@@ -490,27 +460,24 @@ size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items) {
            4 * (size_t)(num_items + 1);
 }
 
+template <int D>
+static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                   const DecodeArgs &a, size_t smem, cudaStream_t stream) {
+    const int ncw = a.heads_per_cta * a.warps_per_head;
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(paged_decode_kernel<D>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
+                   v_map, a);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(paged_decode_merge_kernel<D>, dim3(a.grid, kMergeRowSplit), dim3(256), 0,
+                      stream, a);
+}
+
 cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                 const DecodeArgs &a, size_t smem, cudaStream_t stream) {
-    const int ncw = a.heads_per_cta * a.warps_per_head;
-    const dim3 block((ncw + 1) * 32);
-    cudaError_t e;
-    if (head_dim == 128) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        paged_decode_kernel<128><<<a.grid, block, smem, stream>>>(k_map, v_map, a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        paged_decode_merge_kernel<128><<<a.grid, 256, 0, stream>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(paged_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        paged_decode_kernel<64><<<a.grid, block, smem, stream>>>(k_map, v_map, a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        paged_decode_merge_kernel<64><<<a.grid, 256, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    return head_dim == 128 ? launch_decode_d<128>(k_map, v_map, a, smem, stream)
+                           : launch_decode_d<64>(k_map, v_map, a, smem, stream);
 }
 
 }  // namespace pkv

@@ -22,6 +22,7 @@
 //  * A producer warp streams each key block (K, then V, of one KV head: 16 rows x
 //    head_dim) with TMA into a ring of 128-byte-swizzled shared-memory stages.
 //  * Waits are bounded in time; no CTA waits on another CTA.
+#include "attn_block.cuh"
 #include "paged_prefill.cuh"
 #include "pkv_split.cuh"
 
@@ -41,7 +42,6 @@ struct SeqTiles {
     bool causal;
     int64_t per_head;                  // units of one KV head: sum over tiles
 
-    __device__ __forceinline__ int64_t ntiles() const { return nfull + (rem > 0 ? 1 : 0); }
     // units before tile qt (qt <= nfull)
     __device__ __forceinline__ int64_t before(int64_t qt) const {
         return causal ? qt * A + B * qt * (qt + 1) / 2 : qt * nk_all;
@@ -200,6 +200,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
         tma_prefetch_desc(&k_map);
         tma_prefetch_desc(&v_map);
     }
+    pdl_wait();
+    pdl_trigger();
     build_seq_prefix(a, pre, scan_tmp);
     const int64_t T = pre[a.num_seqs];
     if (blockIdx.x == 0)
@@ -243,8 +245,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
                         const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
 #pragma unroll
                         for (int dc = 0; dc < DCH; ++dc)
-                            tma_load_4d(dst + dc * (kBS * 128), map, &full[stage], 0, dc, h,
-                                        b * kBS, policy);
+                            tma_load_5d(dst + dc * (kBS * 128), map, &full[stage], 0, 0, h, dc,
+                                        b, policy);
                         ++issued;
                         if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
                     }
@@ -272,8 +274,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
     const int g_row = lane >> 2, q4 = lane & 3;
     const int ra = warp * 16 + g_row, rb = ra + 8;  // this lane's two tile rows
     const uint32_t smem_base = smem_u32(smem);
+    const float sl2 = a.scale_log2;
     uint32_t stage = 0, phase = 0;
     int64_t f = lo;
+    RowState<D> st;
     while (f < hi) {
         UnitPos u;
         locate(a, pre, f, u);
@@ -284,9 +288,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
         const bool va = ra < rows && tok_a < tile_tokens;
         const bool vb = rb < rows && tok_b < tile_tokens;
         const int64_t first_pos = (int64_t)(u.t.ctx - u.t.q_len) + u.qt * TPT;
-        const int64_t pos_a = first_pos + min(tok_a, tile_tokens - 1);
-        const int64_t pos_b = first_pos + min(tok_b, tile_tokens - 1);
         const int ctx = u.t.ctx;
+        // keys a row may see: [0, lim)
+        const int64_t lim_a = a.causal ? min64(first_pos + min(tok_a, tile_tokens - 1) + 1, ctx) : ctx;
+        const int64_t lim_b = a.causal ? min64(first_pos + min(tok_b, tile_tokens - 1) + 1, ctx) : ctx;
+        // keys every row of the warp may see (for the no-mask fast path)
+        const int64_t lim_warp = a.causal
+            ? min64(first_pos + min((warp * 16) / group, tile_tokens - 1) + 1, ctx) : ctx;
 
         uint32_t qa[KSTEPS][4];
         {
@@ -305,108 +313,43 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
                 qa[ks][3] = vb ? __ldg(pb + (col + 8) / 2) : 0u;
             }
         }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float o[NT_D][4];
-#pragma unroll
-        for (int n = 0; n < NT_D; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        st.reset();
 
         bool ok = true;
         for (; f < seg_end; ++f) {
-            const int64_t kb = f - u.tile_begin;
-            const int64_t key0 = kb * kBS;
+            const int64_t key0 = (f - u.tile_begin) * kBS;
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            const uint32_t kbase = smem_base + stage * kStageBytes;
             float sacc[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-            {
-                const int mat = lane >> 3, r = lane & 7;
-                const int tok = ((mat >> 1) << 3) + r;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    const int col = ks * 16 + ((mat & 1) << 3);
-                    const uint32_t addr = kbase + (col >> 6) * (kBS * 128) + swz128(tok, col & 63);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(sacc[0], qa[ks], b0, b1);
-                    mma_bf16_16816(sacc[1], qa[ks], b2, b3);
-                }
-            }
+            qk_block<D>(sacc, qa, smem_base + stage * kStageBytes, kBS * 128, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
 
-            // scale, causal / context mask, online softmax (base 2)
-            const int64_t lim_a = a.causal ? min64(pos_a + 1, ctx) : ctx;
-            const int64_t lim_b = a.causal ? min64(pos_b + 1, ctx) : ctx;
-            float mx0 = m0, mx1 = m1;
+            if (key0 + kBS <= lim_warp) {  // the whole block is visible to every row
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int64_t key = key0 + nt * 8 + 2 * q4 + e;
-                    sacc[nt][e] = key < lim_a ? sacc[nt][e] * a.scale_log2 : -INFINITY;
-                    sacc[nt][2 + e] = key < lim_b ? sacc[nt][2 + e] * a.scale_log2 : -INFINITY;
-                    mx0 = fmaxf(mx0, sacc[nt][e]);
-                    mx1 = fmaxf(mx1, sacc[nt][2 + e]);
+                for (int i = 0; i < 4; ++i) {
+                    sacc[0][i] *= sl2;
+                    sacc[1][i] *= sl2;
                 }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int64_t key = key0 + nt * 8 + 2 * q4 + e;
+                        sacc[nt][e] = key < lim_a ? sacc[nt][e] * sl2 : -INFINITY;
+                        sacc[nt][2 + e] = key < lim_b ? sacc[nt][2 + e] * sl2 : -INFINITY;
+                    }
             }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            // A row with nothing visible yet keeps m = -inf; subtract 0 instead so
-            // that no -inf - -inf appears.
-            const float base0 = mx0 == -INFINITY ? 0.f : mx0;
-            const float base1 = mx1 == -INFINITY ? 0.f : mx1;
-            const float alpha0 = fast_exp2(m0 - base0), alpha1 = fast_exp2(m1 - base1);
-            m0 = mx0;
-            m1 = mx1;
             uint32_t pa[4];
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t p01 = pack_bf16x2(fast_exp2(sacc[nt][0] - base0), fast_exp2(sacc[nt][1] - base0));
-                const uint32_t p23 = pack_bf16x2(fast_exp2(sacc[nt][2] - base1), fast_exp2(sacc[nt][3] - base1));
-                ps0 += bf16_lo(p01) + bf16_hi(p01);
-                ps1 += bf16_lo(p23) + bf16_hi(p23);
-                pa[nt * 2 + 0] = p01;
-                pa[nt * 2 + 1] = p23;
-            }
-            l0 = l0 * alpha0 + ps0;
-            l1 = l1 * alpha1 + ps1;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                o[n][0] *= alpha0;
-                o[n][1] *= alpha0;
-                o[n][2] *= alpha1;
-                o[n][3] *= alpha1;
-            }
+            softmax_update<D>(st, sacc, pa);
 
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            const uint32_t vbase = smem_base + stage * kStageBytes;
-            {
-                const int valid = (int)min64(kBS, ctx - key0);
-                const int mat = lane >> 3, r = lane & 7;
-                const int tok = ((mat & 1) << 3) + r;
-                const uint32_t keep_lo = (2 * q4 < valid ? 0x0000ffffu : 0u) |
-                                         (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-                const uint32_t keep_hi = (8 + 2 * q4 < valid ? 0x0000ffffu : 0u) |
-                                         (8 + 2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int n2 = 0; n2 < NT_D / 2; ++n2) {
-                    const int col = n2 * 16 + ((mat >> 1) << 3);
-                    const uint32_t addr = vbase + (col >> 6) * (kBS * 128) + swz128(tok, col & 63);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                    b0 &= keep_lo;
-                    b1 &= keep_hi;
-                    b2 &= keep_lo;
-                    b3 &= keep_hi;
-                    mma_bf16_16816(o[2 * n2], pa, b0, b1);
-                    mma_bf16_16816(o[2 * n2 + 1], pa, b2, b3);
-                }
-            }
+            if (key0 + kBS <= ctx)
+                pv_block<D, false>(st, pa, smem_base + stage * kStageBytes, kBS * 128, kBS, lane);
+            else
+                pv_block<D, true>(st, pa, smem_base + stage * kStageBytes, kBS * 128,
+                                  (int)(ctx - key0), lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
@@ -417,13 +360,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
             return;
         }
 
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        finish_sums<D>(st);
         const bool whole = lo <= u.tile_begin && seg_end == tile_end;
         if (whole) {
-            const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+            const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
             const int64_t qrow_a = u.t.q_row0 + u.qt * TPT + tok_a;
             const int64_t qrow_b = u.t.q_row0 + u.qt * TPT + tok_b;
             __nv_bfloat16 *oa = a.out + (qrow_a * a.num_heads + (int64_t)u.kvh * group + ra % group) * D;
@@ -431,8 +371,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
 #pragma unroll
             for (int n = 0; n < NT_D; ++n) {
                 const int col = n * 8 + 2 * q4;
-                if (va) *reinterpret_cast<uint32_t *>(oa + col) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
-                if (vb) *reinterpret_cast<uint32_t *>(ob + col) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+                if (va) *reinterpret_cast<uint32_t *>(oa + col) = pack_bf16x2(st.o[n][0] * inv0, st.o[n][1] * inv0);
+                if (vb) *reinterpret_cast<uint32_t *>(ob + col) = pack_bf16x2(st.o[n][2] * inv1, st.o[n][3] * inv1);
             }
         } else {
             const int slot = part_slot(c, u.tile_begin, T, ge);
@@ -441,31 +381,41 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
 #pragma unroll
             for (int n = 0; n < NT_D; ++n) {
                 const int col = n * 8 + 2 * q4;
-                if (va) *reinterpret_cast<float2 *>(ws + (int64_t)ra * D + col) = make_float2(o[n][0], o[n][1]);
-                if (vb) *reinterpret_cast<float2 *>(ws + (int64_t)rb * D + col) = make_float2(o[n][2], o[n][3]);
+                if (va) *reinterpret_cast<float2 *>(ws + (int64_t)ra * D + col) = make_float2(st.o[n][0], st.o[n][1]);
+                if (vb) *reinterpret_cast<float2 *>(ws + (int64_t)rb * D + col) = make_float2(st.o[n][2], st.o[n][3]);
             }
             if (q4 == 0) {
-                if (va) ml[ra] = make_float2(m0, l0);
-                if (vb) ml[rb] = make_float2(m1, l1);
+                if (va) ml[ra] = make_float2(st.m0, st.l0);
+                if (vb) ml[rb] = make_float2(st.m1, st.l1);
             }
         }
         f = seg_end;
     }
 }
 
-// Merge kernel: CTA b merges the tile split at the boundary between CTA b and b+1 if
-// that boundary is the tile's first split; it also writes zero rows for prefill
-// sequences whose metadata was invalid (flagged by the main kernel).
+// Merge kernel, grid (grid, kMergeRowSplit): CTA (b, y) merges rows y, y + Y, ... of
+// the tile split at the boundary between CTA shares b and b+1 if that boundary is the
+// tile's first split (o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p).  The CTAs
+// with y == 0 also write zero rows for prefill sequences whose metadata was invalid.
+constexpr int kMergeRowSplit = 4;
+constexpr int kMergeMaxRows = 32;
+constexpr int kMergeSmemParts = 16;  // weights of the first parts kept in shared memory
+
 template <int D>
 __global__ void __launch_bounds__(256)
 paged_prefill_merge_kernel(const PrefillArgs a) {
+    __shared__ float s_w[kMergeMaxRows][kMergeSmemParts];
+    __shared__ float s_base[kMergeMaxRows], s_inv[kMergeMaxRows];
+    pdl_wait();
     const int64_t *pre = a.ws_seq_prefix;
     const int S = a.num_seqs;
-    for (int s = blockIdx.x; s < S; s += gridDim.x) {
-        const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-        if (q1 - q0 < 2 || q0 < 0 || q1 > a.total_q || pre[s + 1] != pre[s]) continue;
-        for (int64_t i = threadIdx.x; i < (int64_t)(q1 - q0) * a.num_heads * D / 2; i += blockDim.x)
-            reinterpret_cast<uint32_t *>(a.out + (int64_t)q0 * a.num_heads * D)[i] = 0u;
+    if (blockIdx.y == 0) {
+        for (int s = blockIdx.x; s < S; s += gridDim.x) {
+            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+            if (q1 - q0 < 2 || q0 < 0 || q1 > a.total_q || pre[s + 1] != pre[s]) continue;
+            for (int64_t i = threadIdx.x; i < (int64_t)(q1 - q0) * a.num_heads * D / 2; i += blockDim.x)
+                reinterpret_cast<uint32_t *>(a.out + (int64_t)q0 * a.num_heads * D)[i] = 0u;
+        }
     }
     const int64_t T = pre[S];
     if (T == 0) return;
@@ -478,37 +428,53 @@ paged_prefill_merge_kernel(const PrefillArgs a) {
     if (u.kb == 0) return;                            // boundary between tiles
     if (u.tile_begin < share_begin(b, T, ge)) return;  // merged by an earlier CTA
     const int c0 = b, c1 = share_owner(u.tile_begin + u.tile_blocks - 1, T, ge);
+    const int nparts = c1 - c0 + 1;
     const int group = a.group, TPT = a.tokens_per_tile, rows = TPT * group;
     const int tile_tokens = (int)min64(TPT, u.t.q_len - u.qt * TPT);
-    constexpr int D4 = D / 4;
-    for (int task = threadIdx.x; task < tile_tokens * group * D4; task += blockDim.x) {
-        const int row = task / D4, d4 = task - row * D4;
+    const int live_rows = tile_tokens * group;
+    const int my_rows = (live_rows - (int)blockIdx.y + kMergeRowSplit - 1) / kMergeRowSplit;
+    for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
+        const int row = blockIdx.y + k * kMergeRowSplit;
         float M = -INFINITY;
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int slot = part_slot(cc, u.tile_begin, T, ge);
-            M = fmaxf(M, a.ws_ml[(int64_t)slot * rows + row].x);
-        }
+        for (int p = 0; p < nparts; ++p)
+            M = fmaxf(M, a.ws_ml[(int64_t)part_slot(c0 + p, u.tile_begin, T, ge) * rows + row].x);
         const float base = M == -INFINITY ? 0.f : M;
         float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = c0; cc <= c1; ++cc) {
-            const int slot = part_slot(cc, u.tile_begin, T, ge);
-            const float2 ml = a.ws_ml[(int64_t)slot * rows + row];
+        for (int p = 0; p < nparts; ++p) {
+            const float2 ml = a.ws_ml[(int64_t)part_slot(c0 + p, u.tile_begin, T, ge) * rows + row];
             const float w = fast_exp2(ml.x - base);
             L += w * ml.y;
+            if (p < kMergeSmemParts) s_w[k][p] = w;
+        }
+        const float inv = 1.f / L;
+        for (int p = 0; p < nparts && p < kMergeSmemParts; ++p) s_w[k][p] *= inv;
+        s_base[k] = base;
+        s_inv[k] = inv;
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
+        const int k = task / D4, d4 = task - k * D4;
+        const int row = blockIdx.y + k * kMergeRowSplit;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int p = 0; p < nparts; ++p) {
+            const int slot = part_slot(c0 + p, u.tile_begin, T, ge);
+            const float w = p < kMergeSmemParts
+                                ? s_w[k][p]
+                                : fast_exp2(a.ws_ml[(int64_t)slot * rows + row].x - s_base[k]) * s_inv[k];
             const float4 ov = reinterpret_cast<const float4 *>(a.ws_o + ((int64_t)slot * rows + row) * D)[d4];
             acc.x += w * ov.x;
             acc.y += w * ov.y;
             acc.z += w * ov.z;
             acc.w += w * ov.w;
         }
-        const float inv = 1.f / L;
         const int tok = row / group, hg = row - tok * group;
         const int64_t qrow = u.t.q_row0 + u.qt * TPT + tok;
         __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)u.kvh * group + hg) * D;
         uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
         reinterpret_cast<uint2 *>(orow)[d4] = packed;
     }
 }
@@ -523,7 +489,7 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     p->tokens_per_tile = 16 * (8 / p->group);
     p->rows = p->tokens_per_tile * p->group;
     p->warps = (p->rows + 15) / 16;
-    p->grid = sms;
+    p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
     p->stage_bytes = kBS * head_dim * 2;
     const size_t fixed = 1024 + 34 * 8 + 8 * (size_t)(num_seqs + 1) + 8;
@@ -540,24 +506,23 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     return PKV_OK;
 }
 
+template <int D>
+static cudaError_t launch_prefill_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
+                                    const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(paged_prefill_kernel<D>, dim3(a.grid), dim3((p.warps + 1) * 32), p.smem, stream,
+                   k_map, v_map, a);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(paged_prefill_merge_kernel<D>, dim3(a.grid, kMergeRowSplit), dim3(256), 0,
+                      stream, a);
+}
+
 cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                  const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream) {
-    const dim3 block((p.warps + 1) * 32);
-    cudaError_t e;
-    if (head_dim == 128) {
-        e = cudaFuncSetAttribute(paged_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (e != cudaSuccess) return e;
-        paged_prefill_kernel<128><<<a.grid, block, p.smem, stream>>>(k_map, v_map, a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        paged_prefill_merge_kernel<128><<<a.grid, 256, 0, stream>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(paged_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (e != cudaSuccess) return e;
-        paged_prefill_kernel<64><<<a.grid, block, p.smem, stream>>>(k_map, v_map, a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        paged_prefill_merge_kernel<64><<<a.grid, 256, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    return head_dim == 128 ? launch_prefill_d<128>(k_map, v_map, a, p, stream)
+                           : launch_prefill_d<64>(k_map, v_map, a, p, stream);
 }
 
 }  // namespace pkv
