@@ -102,7 +102,7 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, in
 struct DecodePlan {
     int group, warps_per_head, heads_per_cta, head_tiles, items, stage_bytes, num_stages, grid;
     size_t smem;
-    size_t off_prefix, off_ml, off_o, bytes;
+    size_t off_jobs, off_ml, off_o, bytes;
 };
 
 int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, const DeviceInfo &d,
@@ -121,14 +121,14 @@ int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, con
     const size_t fixed = pkv::decode_smem_bytes(0, 0, p->items);
     const int budget = d.smem_optin;
     int nst = (int)((budget - (int64_t)fixed) / (p->stage_bytes + 16));
-    if (nst > 12) nst = 12;
+    if (nst > 6) nst = 6;  // deeper rings measured no faster; the rest is left free
     if (nst < 2) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
     p->smem = pkv::decode_smem_bytes(p->stage_bytes, nst, p->items);
     p->grid = d.sms < 256 ? d.sms : 256;  // the merge kernels hold <= 256 parts per item
     const size_t rows = (size_t)ht * p->group;
-    p->off_prefix = 0;
-    p->off_ml = round_up(4 * (size_t)(p->items + 1), 256);
+    p->off_jobs = 0;
+    p->off_ml = round_up(sizeof(pkv::MergeJob) * (size_t)p->grid, 256);
     p->off_o = p->off_ml + round_up(2 * (size_t)p->grid * rows * 8, 256);
     p->bytes = p->off_o + round_up(2 * (size_t)p->grid * rows * head_dim * 4, 256);
     return PKV_OK;
@@ -184,7 +184,7 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     a.min_blocks_per_cta = 8;
     a.num_blocks = num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.ws_prefix = reinterpret_cast<int32_t *>(ws + p.off_prefix);
+    a.ws_jobs = reinterpret_cast<pkv::MergeJob *>(ws + p.off_jobs);
     a.ws_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
     a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
     a.err = d.err;
@@ -356,7 +356,7 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     a.num_blocks = num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
     uint8_t *pws = ws + round_up(p.bytes, 256);
-    a.ws_seq_prefix = reinterpret_cast<int64_t *>(pws + pp.off_seq_prefix);
+    a.ws_jobs = reinterpret_cast<pkv::MergeJob *>(pws + pp.off_jobs);
     a.ws_ml = reinterpret_cast<float2 *>(pws + pp.off_ml);
     a.ws_o = reinterpret_cast<float *>(pws + pp.off_o);
     a.max_seqs = num_seqs;

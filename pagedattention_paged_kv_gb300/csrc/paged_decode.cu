@@ -25,6 +25,7 @@
 //  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
 //    reports PKV_DEVERR_TIMEOUT instead of hanging.
 #include "attn_block.cuh"
+#include "merge.cuh"
 #include "paged_decode.cuh"
 #include "pkv_split.cuh"
 
@@ -106,6 +107,49 @@ __device__ __forceinline__ int find_item(const int32_t *pre, int V, int64_t f) {
 
 }  // namespace
 
+// CTA 0: one merge job per boundary between CTA shares (the item split there, when that
+// is its first split), and zero rows for decode rows whose context is empty.
+template <int D>
+__device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pre, int V, int64_t T,
+                                          int ge) {
+    const int rows = a.heads_per_cta * a.group;
+    for (int b = threadIdx.x; b < a.grid; b += blockDim.x) {
+        MergeJob j;
+        no_job(j);
+        if (T > 0 && b < ge - 1) {
+            const int64_t f = share_begin(b + 1, T, ge);
+            const int v = find_item(pre, V, f);
+            const int64_t item_beg = pre[v];
+            if (item_beg != f && item_beg >= share_begin(b, T, ge)) {
+                const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
+                j.item_begin = item_beg;
+                j.total_units = T;
+                j.out_row0 = a.query_start_loc ? a.query_start_loc[s] : s;
+                j.c0 = b;
+                j.c1 = share_owner(pre[v + 1] - 1, T, ge);
+                j.ge = ge;
+                j.rows = rows;
+                j.rows_per_token = rows;
+                j.head0 = ht * rows;
+            }
+        }
+        a.ws_jobs[b] = j;
+    }
+    const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int v = w; v < V; v += nw) {  // one warp per empty item
+        if (pre[v] != pre[v + 1]) continue;
+        const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
+        int64_t qrow = s;
+        if (a.query_start_loc) {
+            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+            if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
+            qrow = q0;
+        }
+        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
+        for (int i = lane; i < rows * D / 2; i += 32) reinterpret_cast<uint32_t *>(orow)[i] = 0u;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(288, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
@@ -149,9 +193,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     build_prefix(a, V, pre, scan_tmp);  // ends with __syncthreads
     const int64_t T = pre[V];
     const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i <= V; i += blockDim.x) a.ws_prefix[i] = pre[i];
-    }
+    if (blockIdx.x == 0) write_jobs_and_empty_rows<D>(a, pre, V, T, ge);
     if ((int)blockIdx.x >= ge || T == 0) return;
     const int c = blockIdx.x;
     const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
@@ -345,113 +387,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 }
 
-// Merge kernel, grid (grid, kMergeRowSplit): CTA (b, y) handles rows y, y + Y, ... of
-// the item split at the boundary between CTA shares b and b+1, if that boundary is the
-// item's first split.  Parts p (one per CTA share that touched the item) combine as
-//     o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,   M = max_p m_p.
-// The CTAs with y == 0 also write zero rows for decode rows whose context is empty.
-constexpr int kMergeRowSplit = 4;
-constexpr int kMergeMaxRows = 32;    // rows per CTA (ceil(rows / kMergeRowSplit) <= 32)
-constexpr int kMergeSmemParts = 16;  // weights of the first parts kept in shared memory
-
-template <int D>
-__global__ void __launch_bounds__(256)
-paged_decode_merge_kernel(const DecodeArgs a) {
-    __shared__ float s_w[kMergeMaxRows][kMergeSmemParts];
-    __shared__ float s_base[kMergeMaxRows], s_inv[kMergeMaxRows];
-    pdl_wait();
-    const int V = a.num_seqs * a.head_tiles;
-    const int32_t *pre = a.ws_prefix;
-    const int64_t T = pre[V];
-    const int rows = a.heads_per_cta * a.group;
-
-    if (blockIdx.y == 0) {
-        for (int v = blockIdx.x; v < V; v += gridDim.x) {
-            if (pre[v] != pre[v + 1]) continue;
-            const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
-            int64_t qrow = s;
-            if (a.query_start_loc) {
-                const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-                if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
-                qrow = q0;
-            }
-            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
-            for (int i = threadIdx.x; i < rows * D / 2; i += blockDim.x)
-                reinterpret_cast<uint32_t *>(orow)[i] = 0u;
-        }
-    }
-    if (T == 0) return;
-    const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
-    const int b = blockIdx.x;
-    if (b >= ge - 1) return;
-    const int64_t f = share_begin(b + 1, T, ge);  // first block of CTA b+1
-    int lo = 0, hi = V;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pre[mid] <= f) lo = mid; else hi = mid;
-    }
-    const int v = lo;
-    const int64_t item_beg = pre[v], item_end = pre[v + 1];
-    if (item_beg == f) return;                          // boundary between items
-    if (item_beg < share_begin(b, T, ge)) return;       // split earlier: merged elsewhere
-    const int c0 = b, c1 = share_owner(item_end - 1, T, ge);
-    const int nparts = c1 - c0 + 1;
-    const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
-    const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
-    __nv_bfloat16 *orow0 = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
-
-    // my rows: r = blockIdx.y + k * kMergeRowSplit
-    const int my_rows = (rows - (int)blockIdx.y + kMergeRowSplit - 1) / kMergeRowSplit;
-    // 1) per row: weights w_p = 2^(m_p - M) / sum_q 2^(m_q - M) l_q
-    for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
-        const int row = blockIdx.y + k * kMergeRowSplit;
-        float M = -INFINITY;
-        for (int p = 0; p < nparts; ++p)
-            M = fmaxf(M, a.ws_ml[(int64_t)part_slot(c0 + p, item_beg, T, ge) * rows + row].x);
-        float L = 0.f;
-        for (int p = 0; p < nparts; ++p) {
-            const float2 ml = a.ws_ml[(int64_t)part_slot(c0 + p, item_beg, T, ge) * rows + row];
-            const float w = fast_exp2(ml.x - M);
-            L += w * ml.y;
-            if (p < kMergeSmemParts) s_w[k][p] = w;
-        }
-        const float inv = 1.f / L;
-        for (int p = 0; p < nparts && p < kMergeSmemParts; ++p) s_w[k][p] *= inv;
-        s_base[k] = M;
-        s_inv[k] = inv;
-    }
-    __syncthreads();
-    // 2) weighted sums, 4 columns per task
-    constexpr int D4 = D / 4;
-    for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
-        const int k = task / D4, d4 = task - k * D4;
-        const int row = blockIdx.y + k * kMergeRowSplit;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int p = 0; p < nparts; ++p) {
-            const int slot = part_slot(c0 + p, item_beg, T, ge);
-            const float w = p < kMergeSmemParts
-                                ? s_w[k][p]
-                                : fast_exp2(a.ws_ml[(int64_t)slot * rows + row].x - s_base[k]) * s_inv[k];
-            const float4 ov = reinterpret_cast<const float4 *>(a.ws_o + ((int64_t)slot * rows + row) * D)[d4];
-            acc.x += w * ov.x;
-            acc.y += w * ov.y;
-            acc.z += w * ov.z;
-            acc.w += w * ov.w;
-        }
-        uint2 packed;
-        packed.x = pack_bf16x2(acc.x, acc.y);
-        packed.y = pack_bf16x2(acc.z, acc.w);
-        reinterpret_cast<uint2 *>(orow0 + (int64_t)row * D)[d4] = packed;
-    }
-}
-
 template __global__ void paged_decode_kernel<64>(const __grid_constant__ CUtensorMap,
                                                  const __grid_constant__ CUtensorMap, const DecodeArgs);
 template __global__ void paged_decode_kernel<128>(const __grid_constant__ CUtensorMap,
                                                   const __grid_constant__ CUtensorMap, const DecodeArgs);
-template __global__ void paged_decode_merge_kernel<64>(const DecodeArgs);
-template __global__ void paged_decode_merge_kernel<128>(const DecodeArgs);
 
 // ---- host-side launch ----------------------------------------------------------
 
@@ -470,8 +409,14 @@ static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &
     e = launch_pdl(paged_decode_kernel<D>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
                    v_map, a);
     if (e != cudaSuccess) return e;
-    return launch_pdl(paged_decode_merge_kernel<D>, dim3(a.grid, kMergeRowSplit), dim3(256), 0,
-                      stream, a);
+    MergeArgs m;
+    m.jobs = a.ws_jobs;
+    m.ws_ml = a.ws_ml;
+    m.ws_o = a.ws_o;
+    m.out = a.out;
+    m.slot_rows = a.heads_per_cta * a.group;
+    m.num_heads = a.num_heads;
+    return launch_merge<D>(m, a.grid, stream);
 }
 
 cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,

@@ -1,6 +1,7 @@
 // paged_decode.cuh -- arguments and launcher of the decode kernel (paged_decode.cu).
 #pragma once
 
+#include "merge.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -27,7 +28,7 @@ struct DecodeArgs {
     int min_blocks_per_cta;
     int64_t num_blocks;
     float scale_log2;    // scale * log2(e)
-    int32_t *ws_prefix;  // [items + 1]
+    MergeJob *ws_jobs;   // [grid]
     float2 *ws_ml;       // [2 * grid][heads_per_cta * group]  (running max, sum)
     float *ws_o;         // [2 * grid][heads_per_cta * group][head_dim]
     int *err;            // device error word

@@ -23,6 +23,7 @@
 //    head_dim) with TMA into a ring of 128-byte-swizzled shared-memory stages.
 //  * Waits are bounded in time; no CTA waits on another CTA.
 #include "attn_block.cuh"
+#include "merge.cuh"
 #include "paged_prefill.cuh"
 #include "pkv_split.cuh"
 
@@ -164,6 +165,42 @@ __device__ __forceinline__ void locate(const PrefillArgs &a, const int64_t *pre,
 
 }  // namespace
 
+// CTA 0: one merge job per boundary between CTA shares (the tile split there, when
+// that is its first split), and zero rows for prefill sequences whose metadata was
+// invalid (their units were dropped from the split).
+template <int D>
+__device__ void write_jobs_and_invalid_rows(const PrefillArgs &a, const int64_t *pre, int64_t T,
+                                            int ge) {
+    for (int b = threadIdx.x; b < a.grid; b += blockDim.x) {
+        MergeJob j;
+        no_job(j);
+        if (T > 0 && b < ge - 1) {
+            const int64_t f = share_begin(b + 1, T, ge);
+            UnitPos u;
+            locate(a, pre, f, u);
+            if (u.kb != 0 && u.tile_begin >= share_begin(b, T, ge)) {
+                j.item_begin = u.tile_begin;
+                j.total_units = T;
+                j.out_row0 = u.t.q_row0 + u.qt * a.tokens_per_tile;
+                j.c0 = b;
+                j.c1 = share_owner(u.tile_begin + u.tile_blocks - 1, T, ge);
+                j.ge = ge;
+                j.rows = (int)min64(a.tokens_per_tile, u.t.q_len - u.qt * a.tokens_per_tile) * a.group;
+                j.rows_per_token = a.group;
+                j.head0 = u.kvh * a.group;
+            }
+        }
+        a.ws_jobs[b] = j;
+    }
+    const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int s = w; s < a.num_seqs; s += nw) {  // one warp per dropped sequence
+        const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
+        if (q1 - q0 < 2 || q0 < 0 || q1 > a.total_q || pre[s + 1] != pre[s]) continue;
+        uint32_t *o = reinterpret_cast<uint32_t *>(a.out + (int64_t)q0 * a.num_heads * D);
+        for (int64_t i = lane; i < (int64_t)(q1 - q0) * a.num_heads * D / 2; i += 32) o[i] = 0u;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(288, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
@@ -204,9 +241,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
     pdl_trigger();
     build_seq_prefix(a, pre, scan_tmp);
     const int64_t T = pre[a.num_seqs];
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i <= a.num_seqs; i += blockDim.x) a.ws_seq_prefix[i] = pre[i];
     const int ge = split_ctas(T, a.grid, 4);
+    if (blockIdx.x == 0) write_jobs_and_invalid_rows<D>(a, pre, T, ge);
     if ((int)blockIdx.x >= ge || T == 0) return;
     const int c = blockIdx.x;
     const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
@@ -393,92 +429,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 }
 
-// Merge kernel, grid (grid, kMergeRowSplit): CTA (b, y) merges rows y, y + Y, ... of
-// the tile split at the boundary between CTA shares b and b+1 if that boundary is the
-// tile's first split (o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p).  The CTAs
-// with y == 0 also write zero rows for prefill sequences whose metadata was invalid.
-constexpr int kMergeRowSplit = 4;
-constexpr int kMergeMaxRows = 32;
-constexpr int kMergeSmemParts = 16;  // weights of the first parts kept in shared memory
-
-template <int D>
-__global__ void __launch_bounds__(256)
-paged_prefill_merge_kernel(const PrefillArgs a) {
-    __shared__ float s_w[kMergeMaxRows][kMergeSmemParts];
-    __shared__ float s_base[kMergeMaxRows], s_inv[kMergeMaxRows];
-    pdl_wait();
-    const int64_t *pre = a.ws_seq_prefix;
-    const int S = a.num_seqs;
-    if (blockIdx.y == 0) {
-        for (int s = blockIdx.x; s < S; s += gridDim.x) {
-            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-            if (q1 - q0 < 2 || q0 < 0 || q1 > a.total_q || pre[s + 1] != pre[s]) continue;
-            for (int64_t i = threadIdx.x; i < (int64_t)(q1 - q0) * a.num_heads * D / 2; i += blockDim.x)
-                reinterpret_cast<uint32_t *>(a.out + (int64_t)q0 * a.num_heads * D)[i] = 0u;
-        }
-    }
-    const int64_t T = pre[S];
-    if (T == 0) return;
-    const int ge = split_ctas(T, a.grid, 4);
-    const int b = blockIdx.x;
-    if (b >= ge - 1) return;
-    const int64_t f = share_begin(b + 1, T, ge);
-    UnitPos u;
-    locate(a, pre, f, u);
-    if (u.kb == 0) return;                            // boundary between tiles
-    if (u.tile_begin < share_begin(b, T, ge)) return;  // merged by an earlier CTA
-    const int c0 = b, c1 = share_owner(u.tile_begin + u.tile_blocks - 1, T, ge);
-    const int nparts = c1 - c0 + 1;
-    const int group = a.group, TPT = a.tokens_per_tile, rows = TPT * group;
-    const int tile_tokens = (int)min64(TPT, u.t.q_len - u.qt * TPT);
-    const int live_rows = tile_tokens * group;
-    const int my_rows = (live_rows - (int)blockIdx.y + kMergeRowSplit - 1) / kMergeRowSplit;
-    for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
-        const int row = blockIdx.y + k * kMergeRowSplit;
-        float M = -INFINITY;
-        for (int p = 0; p < nparts; ++p)
-            M = fmaxf(M, a.ws_ml[(int64_t)part_slot(c0 + p, u.tile_begin, T, ge) * rows + row].x);
-        const float base = M == -INFINITY ? 0.f : M;
-        float L = 0.f;
-        for (int p = 0; p < nparts; ++p) {
-            const float2 ml = a.ws_ml[(int64_t)part_slot(c0 + p, u.tile_begin, T, ge) * rows + row];
-            const float w = fast_exp2(ml.x - base);
-            L += w * ml.y;
-            if (p < kMergeSmemParts) s_w[k][p] = w;
-        }
-        const float inv = 1.f / L;
-        for (int p = 0; p < nparts && p < kMergeSmemParts; ++p) s_w[k][p] *= inv;
-        s_base[k] = base;
-        s_inv[k] = inv;
-    }
-    __syncthreads();
-    constexpr int D4 = D / 4;
-    for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
-        const int k = task / D4, d4 = task - k * D4;
-        const int row = blockIdx.y + k * kMergeRowSplit;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int p = 0; p < nparts; ++p) {
-            const int slot = part_slot(c0 + p, u.tile_begin, T, ge);
-            const float w = p < kMergeSmemParts
-                                ? s_w[k][p]
-                                : fast_exp2(a.ws_ml[(int64_t)slot * rows + row].x - s_base[k]) * s_inv[k];
-            const float4 ov = reinterpret_cast<const float4 *>(a.ws_o + ((int64_t)slot * rows + row) * D)[d4];
-            acc.x += w * ov.x;
-            acc.y += w * ov.y;
-            acc.z += w * ov.z;
-            acc.w += w * ov.w;
-        }
-        const int tok = row / group, hg = row - tok * group;
-        const int64_t qrow = u.t.q_row0 + u.qt * TPT + tok;
-        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)u.kvh * group + hg) * D;
-        uint2 packed;
-        packed.x = pack_bf16x2(acc.x, acc.y);
-        packed.y = pack_bf16x2(acc.z, acc.w);
-        reinterpret_cast<uint2 *>(orow)[d4] = packed;
-    }
-}
-
 // ---- host side -------------------------------------------------------------------
 
 int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
@@ -499,8 +449,8 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     p->num_stages = nst;
     p->smem = fixed + (size_t)nst * (p->stage_bytes + 16);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    p->off_seq_prefix = 0;
-    p->off_ml = up(8 * (size_t)(num_seqs + 1));
+    p->off_jobs = 0;
+    p->off_ml = up(sizeof(MergeJob) * (size_t)p->grid);
     p->off_o = p->off_ml + up(2 * (size_t)p->grid * p->rows * 8);
     p->ws_bytes = p->off_o + up(2 * (size_t)p->grid * p->rows * head_dim * 4);
     return PKV_OK;
@@ -515,8 +465,14 @@ static cudaError_t launch_prefill_d(const CUtensorMap &k_map, const CUtensorMap 
     e = launch_pdl(paged_prefill_kernel<D>, dim3(a.grid), dim3((p.warps + 1) * 32), p.smem, stream,
                    k_map, v_map, a);
     if (e != cudaSuccess) return e;
-    return launch_pdl(paged_prefill_merge_kernel<D>, dim3(a.grid, kMergeRowSplit), dim3(256), 0,
-                      stream, a);
+    MergeArgs m;
+    m.jobs = a.ws_jobs;
+    m.ws_ml = a.ws_ml;
+    m.ws_o = a.ws_o;
+    m.out = a.out;
+    m.slot_rows = p.rows;
+    m.num_heads = a.num_heads;
+    return launch_merge<D>(m, a.grid, stream);
 }
 
 cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,

@@ -2,6 +2,7 @@
 // (paged_prefill.cu): attention for every sequence of a varlen batch with q_len >= 2.
 #pragma once
 
+#include "merge.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -27,7 +28,7 @@ struct PrefillArgs {
     bool causal;
     int64_t num_blocks;
     float scale_log2;
-    int64_t *ws_seq_prefix;  // [num_seqs + 1] units before each sequence
+    MergeJob *ws_jobs;       // [grid]
     float2 *ws_ml;           // [2 * grid][rows]
     float *ws_o;             // [2 * grid][rows][head_dim]
     int max_seqs;
@@ -37,7 +38,7 @@ struct PrefillArgs {
 struct PrefillPlan {
     int group, tokens_per_tile, rows, warps, grid, num_stages, stage_bytes, max_seqs;
     size_t smem;
-    size_t off_seq_prefix, off_ml, off_o, ws_bytes;
+    size_t off_jobs, off_ml, off_o, ws_bytes;
 };
 
 // Fills *p for these sizes (num_seqs bounds the per-sequence table); PKV_OK or

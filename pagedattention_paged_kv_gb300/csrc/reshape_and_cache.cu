@@ -9,6 +9,7 @@
 // One warp per (token, K-or-V) row: the row (num_kv_heads * head_dim * 2 bytes,
 // 2 KiB for Llama-70B shapes) moves as 16-byte vectors, fully coalesced on both sides.
 // The source is read once (no L1 allocation); the destination is written normally.
+#include "attn_block.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -18,6 +19,8 @@ reshape_and_cache_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cach
                          const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                          const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                          int64_t num_slots, int row_vecs, int *err) {
+    pdl_wait();  // the rows and slots may come from the previous kernel in the stream
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -45,11 +48,10 @@ cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k
     int64_t ctas = (2 * num_tokens + warps_per_cta - 1) / warps_per_cta;
     const int64_t cap = (int64_t)num_sms * 8;
     if (ctas > cap) ctas = cap;
-    reshape_and_cache_kernel<<<(unsigned)ctas, warps_per_cta * 32, 0, stream>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
-        num_slots, row_bytes / 16, err);
-    return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)ctas), dim3(warps_per_cta * 32), 0,
+                      stream, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+                      num_tokens, num_slots, row_bytes / 16, err);
 }
 
 }  // namespace pkv
