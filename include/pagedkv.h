@@ -64,6 +64,7 @@ extern "C" {
 #define PKV_ERR_CUDA                -4  /* a CUDA runtime call or launch failed */
 #define PKV_ERR_OOM                 -5  /* block manager: not enough free blocks */
 #define PKV_ERR_DEVICE_DATA         -6  /* returned by pkv_get_device_error */
+#define PKV_ERR_STATIC_SCRATCH_LIMIT -7 /* sizes need more than PKV_STATIC_SCRATCH_BYTES */
 
 /* ---- flags in the device error word (pkv_get_device_error) ---------------- */
 #define PKV_DEVERR_SLOT         0x1   /* slot_mapping entry >= num_blocks * block_size */
@@ -135,6 +136,34 @@ int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_st
                                int head_dim, int block_size, int64_t num_blocks, float scale,
                                int causal, int dtype, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * Decode attention that allocates nothing and takes no workspace.  The pages have no
+ * counterpart of this call: it exists for callers that are not allowed to allocate
+ * device memory where they run attention -- e.g. a plugin executing inside another
+ * runtime that reserved all device memory up front and forbids later allocations, or
+ * a latency-critical loop that cannot afford cudaMalloc/cudaFree synchronizing the
+ * device -- and that cannot thread a workspace buffer through to this call either.
+ *
+ * It computes exactly what pkv_paged_attention_decode computes, with the same
+ * arguments minus the workspace.  Its scratch space is a fixed array of
+ * PKV_STATIC_SCRATCH_BYTES inside the library's device image: every GPU on which the
+ * library's kernels are loaded holds that array until the process exits.  Sizes whose
+ * scratch would exceed it are refused with PKV_ERR_STATIC_SCRATCH_LIMIT before
+ * anything is launched (pkv_workspace_size(PKV_OP_DECODE, ...) tells what a size
+ * needs).  The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.  All calls on
+ * a device share the one array and it keeps the previous call's contents (nothing in
+ * it has to start at zero), so calls that can overlap on the GPU -- on different
+ * streams, or from different host threads -- race and must not be issued.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int pkv_paged_attention_decode_static(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int num_seqs,
+                                      int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int64_t num_blocks,
+                                      float scale, int dtype, void *stream);
 
 /* Workspace bytes the op needs on the current device for these sizes (0 if the
  * sizes are unsupported).  Does not allocate. */

@@ -204,6 +204,7 @@ extern "C" const char *pkv_status_string(int status) {
         case PKV_ERR_CUDA: return "CUDA error";
         case PKV_ERR_OOM: return "out of blocks";
         case PKV_ERR_DEVICE_DATA: return "invalid device data";
+        case PKV_ERR_STATIC_SCRATCH_LIMIT: return "sizes exceed the static scratch limit";
         default: return "unknown status";
     }
 }
@@ -363,4 +364,65 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     a.err = d->err;
     return pkv::launch_paged_prefill(head_dim, kmap, vmap, a, pp, s) == cudaSuccess ? PKV_OK
                                                                                    : PKV_ERR_CUDA;
+}
+
+// ---- decode with the library's own scratch array (no workspace, no allocation) ----
+//
+// For callers that may not allocate device memory on the path that runs attention
+// (see pkv_paged_attention_decode_static in pagedkv.h): the scratch lives in this
+// fixed-size array of the library's device image instead of a caller buffer.
+
+static __device__ __align__(256) unsigned char g_pkv_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+namespace {
+void *g_static_scratch[kMaxDevices];
+
+// Device address of g_pkv_static_scratch on the current device.  Host code only sees a
+// host-side stand-in under the array's name, so the address has to be looked up (once
+// per device, with that device current) before a kernel may be given it.
+int static_scratch_address(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_static_scratch[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pkv_static_scratch) != cudaSuccess || !p) return PKV_ERR_CUDA;
+        g_static_scratch[dev] = p;
+    }
+    *ptr = g_static_scratch[dev];
+    return PKV_OK;
+}
+}  // namespace
+
+extern "C" int pkv_paged_attention_decode_static(void *out, const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *block_tables,
+                                                 const int32_t *context_lens, int num_seqs,
+                                                 int max_blocks_per_seq, int num_heads,
+                                                 int num_kv_heads, int head_dim, int block_size,
+                                                 int64_t num_blocks, float scale, int dtype,
+                                                 void *stream) {
+    int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, dtype);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    st = device_info(&d);
+    if (st != PKV_OK) return st;
+    DecodePlan p;
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p);
+    if (st != PKV_OK) return st;
+    if (p.bytes > PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_STATIC_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    st = static_scratch_address(&scratch);
+    if (st != PKV_OK) return st;
+    // Every byte the kernels read from the scratch is written earlier in the same call.
+    return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens,
+                      num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
+                      scale, static_cast<uint8_t *>(scratch), PKV_STATIC_SCRATCH_BYTES, *d, p,
+                      static_cast<cudaStream_t>(stream));
 }
