@@ -1,16 +1,20 @@
-"""Benchmark: one paged-KV attention step of the 128-sequence Llama-3.3-70B-shaped
-GQA decode (one layer), on GB300.
+"""Benchmark of the paged-KV attention hot path on GB300.
 
-A step is the whole hot path over one batch: the slot mapping of the step's new
-tokens, the KV write (reshape_and_cache) and decode attention (split-K + merge).
+Default workload (the headline): one decode step of one Llama-3.3-70B-shaped layer
+over 128 sequences -- 64 query heads, 8 KV heads, head_dim 128, 16-token blocks,
+contexts uniform in [500, 2500], blocks scattered by a random permutation of a pool
+with 10% headroom.  A step is the whole hot path over one batch: the slot mapping of
+the step's new tokens (host), the KV write (reshape_and_cache) and decode attention
+(split contexts + log-sum-exp merge).
 
-Prints ONE JSON line (rank 0).  `value` is HBM GB/s of the device-timed step over
-its algorithmic bytes (KV rows read, queries, outputs, new K/V rows, block-table
-entries), with inputs resident in HBM; `e2e` is the same metric through the public
-API with the step's inputs copied from pinned host memory and the output copied
-back inside the timed region.  `--impl reference` times the fp64 CPU oracle on the
-same workload instead.  With --gpus N under torchrun every rank runs its own
-replica (the path has no exchange step), and value sums all ranks' bytes over the
+Prints ONE JSON line (rank 0).  `value` is HBM GB/s over the step's algorithmic bytes
+(every context K/V row once, queries, outputs, new rows, block-table entries) with
+inputs resident in HBM, timed with CUDA events per step and L2 flushed between steps;
+`e2e` is the same metric with the step's inputs copied from pinned host memory (one
+packed copy) and the output copied back inside the timed region.  `--impl reference`
+times the fp64 CPU oracle on the same workload instead.  `--config` selects one of
+the other workloads (reported, not the headline).  Under torchrun every rank runs its
+own replica (the path has no exchange step); value sums the ranks' bytes over the
 slowest rank's time.
 """
 from __future__ import annotations
@@ -32,44 +36,87 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attn: HBM GB/s (% of GB300 peak), seq-steps/s at 128 seqs"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20  # > 126 MB of L2
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--seed", type=int, default=2001)
+    p.add_argument("--config", default="gqa_decode",
+                   choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen"])
+    p.add_argument("--seed", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
 
 
-def peaks():
+WORKLOADS = {
+    "gqa_decode": ("gqa_decode_128seq_llama70b_layer", 2001,
+                   {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
+                    "block_size": 16, "context_lens": "uniform[500,2500]", "pool_headroom": 0.1}),
+    "tiny_decode": ("tiny_decode_4seq", 1001,
+                    {"num_seqs": 4, "num_heads": 4, "num_kv_heads": 4, "head_dim": 64,
+                     "block_size": 16, "context_lens": "uniform[1,100]", "num_blocks": 64}),
+    "skewed_decode": ("skewed_decode_60short_4x32k", 3001,
+                      {"num_seqs": 64, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
+                       "block_size": 16, "context_lens": "60 x uniform[256,2048] + 4 x 32768"}),
+    "mixed_varlen": ("mixed_varlen_512chunk_at_16384_plus_127_decodes", 4001,
+                     {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
+                      "block_size": 16, "chunk": "512 tokens at positions 16384-16895",
+                      "decodes": "127 x context uniform[500,2500]"}),
+}
+
+
+def make_batch(config, seed):
+    from pagedattention_paged_kv_gb300 import workloads as W
+    return {"gqa_decode": W.gqa_decode, "tiny_decode": W.tiny_decode,
+            "skewed_decode": W.skewed_decode, "mixed_varlen": W.mixed_varlen}[config](seed=seed)
+
+
+def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kv_bytes(b):
+    return int(b.context_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * 2
 
 
 def algorithmic_bytes(b):
-    """Bytes the step must move at minimum: every context row of K and V once, the
-    queries and outputs once, the new K/V rows read and written once, and the block
-    table entries and context lengths read once."""
-    Hkv, d, Hq = b.num_kv_heads, b.head_dim, b.num_heads
-    kv = int(b.context_lens.astype(np.int64).sum()) * Hkv * d * 2 * 2
-    qo = 2 * b.q.size * 2
-    new = 2 * 2 * b.k_new.size * 2
+    """(step bytes, attention-call bytes): every context row of K and V once, the
+    queries and outputs once, the new K/V rows read and written once, block-table
+    entries, context lengths and slots read once."""
     nblk = int(((b.context_lens.astype(np.int64) + 15) // 16).sum())
-    meta = nblk * 4 + b.num_seqs * 4 + b.k_new.shape[0] * 8
-    attn = kv + qo + nblk * 4 + b.num_seqs * 4
-    return kv + qo + new + meta, attn
+    attn = kv_bytes(b) + 2 * b.q.size * 2 + nblk * 4 + b.num_seqs * 4
+    if b.query_start_loc is not None:
+        attn += (b.num_seqs + 1) * 4
+    new = 2 * 2 * b.k_new.size * 2 + b.k_new.shape[0] * 8
+    return attn + new, attn
+
+
+def chunk_flops(context_lens, q_lens, head_dim, num_heads):
+    """Causal attention FLOPs of the multi-token rows: 4 * d * Hq per visible
+    (query, key) pair (QK^T and PV, 2 FLOPs per multiply-add)."""
+    pairs = 0
+    for ctx, ql in zip(context_lens, q_lens):
+        ctx, ql = int(ctx), int(ql)
+        if ql < 2:
+            continue
+        first = ctx - ql + 1  # keys seen by the chunk's first row
+        pairs += ql * first + ql * (ql - 1) // 2
+    return 4 * head_dim * num_heads * pairs
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed loop runs."""
+    """nvidia-smi samples of the SM clock and throttle reasons while the timed loop runs."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -84,10 +131,11 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            time.sleep(0.3)  # let the sampler start before the timed loop
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
@@ -125,142 +173,187 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_sha():
+def kernel_source_sha(files):
     h = hashlib.sha256()
-    for f in ("paged_decode.cu", "paged_decode.cuh", "pkv_common.cuh", "pkv_split.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "pagedattention_paged_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """dram bytes per decode launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "pkv_common.cuh",
+                  "pkv_split.cuh", "merge.cuh")
+
+
+def recorded_traffic(name, sources):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{name}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("source_sha") != kernel_source_sha():
+    if d.get("source_sha") != kernel_source_sha(sources):
         return None
     return d
 
 
-def dist_setup(n):
+def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    pg = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
-        pg = dist
-    return rank, world, local, pg
+        return rank, world, local, dist
+    return rank, world, local, None
 
 
-def run_reference(args, rank, world, pg):
-    """Reference arm: the fp64 oracle on the host cores, one bounded sample per step."""
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_step_time(b, seqs):
+    """Times the oracle (as it stands) on the step restricted to `seqs` (all heads),
+    KV write of every new token included.  Returns (seconds, byte share of the sample)."""
     import oracle
-    from pagedattention_paged_kv_gb300 import workloads as W
+    orc = oracle.load()
+    mask = np.zeros(b.q.shape[0], np.uint8)
+    qsl = b.query_start_loc if b.query_start_loc is not None else np.arange(b.num_seqs + 1)
+    for s in seqs:
+        mask[qsl[s]:qsl[s + 1]] = 1
+    share = float(b.context_lens[seqs].astype(np.int64).sum()) / float(b.context_lens.astype(np.int64).sum())
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()
+    t0 = time.perf_counter()
+    slots = orc.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+    orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
+    orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale,
+                        query_start_loc=b.query_start_loc, causal=b.causal, row_mask=mask)
+    return time.perf_counter() - t0, share, orc.num_threads()
+
+
+def sample_seqs(b, n):
+    return np.arange(min(n, b.num_seqs))
+
+
+def run_reference(args, rank):
     if rank != 0:
         return
-    b = W.gqa_decode(seed=args.seed)
-    orc = oracle.load()
-    total_bytes, _ = algorithmic_bytes(b)
-    sample = 16  # sequences per step (all heads)
-    sub = np.arange(sample)
-    mask = np.zeros(b.num_seqs, np.uint8)
-    mask[sub] = 1
-    frac = float(b.context_lens[sub].astype(np.int64).sum()) / float(b.context_lens.astype(np.int64).sum())
-
-    def step():
-        slots = orc.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, 16)
-        kc, vc = b.k_cache, b.v_cache
-        orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
-        orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale, row_mask=mask)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / args.steps
-    value = total_bytes * frac / dt / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": "gqa_decode_128seq_llama70b_layer", "num_seqs": 128,
-                       "num_heads": 64, "num_kv_heads": 8, "head_dim": 128, "block_size": 16,
-                       "context_lens": "uniform[500,2500] seed 2001"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.num_threads(),
-                             "kind": "oracle",
-                             "sample": f"{sample} of {b.num_seqs} sequences (all heads) per step, "
-                                       f"bytes scaled by their share of the context"},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    seed = args.seed if args.seed is not None else WORKLOADS[args.config][1]
+    b = make_batch(args.config, seed)
+    total, _ = algorithmic_bytes(b)
+    seqs = sample_seqs(b, 16)
+    for _ in range(args.warmup if args.warmup < 3 else 1):
+        oracle_step_time(b, seqs)
+    steps = min(args.steps, 5)
+    times = []
+    for _ in range(steps):
+        dt, share, cores = oracle_step_time(b, seqs)
+        times.append(dt)
+    dt = sum(times) / len(times)
+    value = total * share / dt / 1e9
+    name, _, cfg = WORKLOADS[args.config]
+    sample = (f"sequences {seqs[0]}..{seqs[-1]} of {b.num_seqs} (all heads, KV write of every new "
+              f"token) per step; bytes scaled by their share of the total context")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, **cfg, "seed": seed},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
-def cpu_baseline(b, seconds_budget=20.0):
-    """Times the oracle (as it stands) on a bounded sample of the workload."""
-    import oracle
-    orc = oracle.load()
-    total_bytes, _ = algorithmic_bytes(b)
-    sample = 32
-    mask = np.zeros(b.num_seqs, np.uint8)
-    mask[:sample] = 1
-    frac = float(b.context_lens[:sample].astype(np.int64).sum()) / float(b.context_lens.astype(np.int64).sum())
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        slots = orc.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, 16)
-        kc, vc = b.k_cache.copy(), b.v_cache.copy()
-        t1 = time.perf_counter()
-        orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
-        orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale, row_mask=mask)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el > seconds_budget / 4 or reps >= 3:
-            break
-    dt = time.perf_counter() - t1
-    return {"value": total_bytes * frac / dt / 1e9, "unit": "GB/s", "cores": orc.num_threads(),
-            "kind": "oracle",
-            "sample": f"first {sample} of {b.num_seqs} sequences (all heads, KV write of all tokens), "
-                      f"bytes scaled by their share of the total context"}
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+class Packed:
+    """One pinned host buffer and one device buffer with the same layout, holding a
+    step's inputs (q, new K/V rows, slots, block tables, context lengths, and
+    query_start_loc for varlen), so that one copy moves them all."""
+
+    def __init__(self, arrays: dict, device):
+        import torch
+        self.offsets, off = {}, 0
+        for k, a in arrays.items():
+            self.offsets[k] = (off, a.nbytes, a.dtype, a.shape)
+            off = (off + a.nbytes + 255) // 256 * 256
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device=device)
+        hv = self.host.numpy()
+        for k, a in arrays.items():
+            o, n, _, _ = self.offsets[k]
+            hv[o:o + n] = np.frombuffer(np.ascontiguousarray(a).tobytes(), dtype=np.uint8)
+
+    def host_view(self, k):
+        o, n, dt, shape = self.offsets[k]
+        return self.host.numpy()[o:o + n].view(dt).reshape(shape)
+
+    def dev_view(self, k, torch_dtype):
+        o, n, dt, shape = self.offsets[k]
+        return self.dev[o:o + n].view(torch_dtype).view(shape)
 
 
 def main():
     args = parse()
-    rank, world, local, pg = dist_setup(args.gpus)
+    rank, world, local, dist = dist_setup()
     if args.impl == "reference":
-        run_reference(args, rank, world, pg)
+        run_reference(args, rank)
         return
     import torch
     import pagedattention_paged_kv_gb300 as pkv
-    from pagedattention_paged_kv_gb300 import workloads as W
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_helpers import torch_bf16
 
+    name, default_seed, cfg = WORKLOADS[args.config]
+    seed = (args.seed if args.seed is not None else default_seed) + rank
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    b = W.gqa_decode(seed=args.seed + rank)
+    b = make_batch(args.config, seed)
+    varlen = b.query_start_loc is not None
     total_bytes, attn_bytes = algorithmic_bytes(b)
-    S, Hq, d = b.q.shape
-    slots = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, 16)
+    S, Hq, d = b.num_seqs, b.num_heads, b.head_dim
+    T = b.q.shape[0]
+    slots = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
 
-    kc = torch_bf16(b.k_cache, dev)
-    vc = torch_bf16(b.v_cache, dev)
-    q = torch_bf16(b.q, dev)
-    k_new = torch_bf16(b.k_new, dev)
-    v_new = torch_bf16(b.v_new, dev)
-    sm = torch.from_numpy(slots).to(dev)
-    bt = torch.from_numpy(b.block_tables).to(dev)
-    cl = torch.from_numpy(b.context_lens).to(dev)
+    # KV pool: resident state of the serving engine.
+    kc = torch.from_numpy(b.k_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    vc = torch.from_numpy(b.v_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    arrays = {"q": b.q, "k": b.k_new, "v": b.v_new, "slots": slots, "tables": b.block_tables,
+              "ctx": b.context_lens}
+    if varlen:
+        arrays["qsl"] = b.query_start_loc
+    io = Packed(arrays, dev)
+    io.dev.copy_(io.host)
+    q = io.dev_view("q", torch.bfloat16)
+    k_new, v_new = io.dev_view("k", torch.bfloat16), io.dev_view("v", torch.bfloat16)
+    sm = io.dev_view("slots", torch.int64)
+    bt, cl = io.dev_view("tables", torch.int32), io.dev_view("ctx", torch.int32)
+    qsl = io.dev_view("qsl", torch.int32) if varlen else None
+    max_q_len = int(b.q_lens.max())
     out = torch.empty_like(q)
-    ws = torch.empty(pkv.workspace_size(pkv.OP_DECODE, S, S, Hq, b.num_kv_heads, d), dtype=torch.uint8,
-                     device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2 (126 MB)
+    op = pkv.OP_VARLEN if varlen else pkv.OP_DECODE
+    ws = torch.empty(pkv.workspace_size(op, S, T, Hq, b.num_kv_heads, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+
+    def attention(o=out, qq=q, qs=qsl, tables=bt, lens=cl):
+        if varlen:
+            pkv.paged_attention_varlen(o, qq, qs, kc, vc, tables, lens, b.scale, causal=b.causal,
+                                       max_q_len=max_q_len, workspace=ws)
+        else:
+            pkv.paged_attention_decode(o, qq, kc, vc, tables, lens, b.scale, workspace=ws)
 
     def step(ev=None):
         if ev is not None:
@@ -268,109 +361,157 @@ def main():
         pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
         if ev is not None:
             ev[1].record(stream)
-        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, b.scale, workspace=ws)
+        attention()
         if ev is not None:
             ev[2].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
-    assert pkv.get_device_error() == 0
     torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    if pg is not None:
-        pg.barrier()
+    if dist is not None:
+        dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)              # evict the previous step's lines from L2
             step(events[i])
         torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
     attn_ms = [e[1].elapsed_time(e[2]) for e in events]
     kv_ms = [e[0].elapsed_time(e[1]) for e in events]
-    t_step = sum(step_ms) / len(step_ms)
-    if pg is not None:
-        import torch.distributed as dist
-        tt = torch.tensor([t_step], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+    t_step = max_over_ranks(sum(step_ms) / len(step_ms), dist)
     t_attn = sum(attn_ms) / len(attn_ms)
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
     value = total_bytes * world / (t_step * 1e-3) / 1e9
-    peak, peak_kind = peaks()
 
-    # ---- end to end through the public API, host buffers ----
-    hq = torch.from_numpy(b.q.view(np.int16)).pin_memory()
-    hk = torch.from_numpy(b.k_new.view(np.int16)).pin_memory()
-    hv = torch.from_numpy(b.v_new.view(np.int16)).pin_memory()
-    hbt = torch.from_numpy(b.block_tables).pin_memory()
-    hcl = torch.from_numpy(b.context_lens).pin_memory()
-    hout = torch.empty(out.shape, dtype=torch.int16).pin_memory()
-    hsm = torch.empty(len(slots), dtype=torch.int64).pin_memory()
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + hbt.numel() * 4 + hcl.numel() * 4 + hsm.numel() * 8
-    d2h = hout.numel() * 2
+    # ---- end to end through the public API: inputs from pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        h_slots = io.host_view("slots")
 
-    def e2e_step():
-        hsm.numpy()[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, 16)
-        q.view(torch.int16).copy_(hq, non_blocking=True)
-        k_new.view(torch.int16).copy_(hk, non_blocking=True)
-        v_new.view(torch.int16).copy_(hv, non_blocking=True)
-        bt.copy_(hbt, non_blocking=True)
-        cl.copy_(hcl, non_blocking=True)
-        sm.copy_(hsm, non_blocking=True)
-        pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
-        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, b.scale, workspace=ws)
-        hout.copy_(out.view(torch.int16), non_blocking=True)
-        stream.synchronize()
+        def e2e_step():
+            h_slots[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+            io.dev.copy_(io.host, non_blocking=True)
+            pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
+            attention()
+            hout.copy_(out, non_blocking=True)
+            stream.synchronize()
 
-    for _ in range(3):
-        e2e_step()
-    e2e_times = []
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        e2e_step()
-        e2e_times.append(time.perf_counter() - t0)
-    t_e2e = sum(e2e_times) / len(e2e_times)
-    if pg is not None:
-        import torch.distributed as dist
-        tt = torch.tensor([t_e2e], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+        for _ in range(5):
+            e2e_step()
+        n_e2e = min(args.steps, 500)
+        times = []
+        for i in range(n_e2e):
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            times.append(time.perf_counter() - t0)
+        t_e2e = max_over_ranks(sum(times) / len(times), dist)
+        e2e = {"value": total_bytes * world / t_e2e / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": io.nbytes, "d2h_bytes_per_step": hout.numel() * 2,
+               "ms_per_step": t_e2e * 1e3, "steps": n_e2e}
+
+    # ---- varlen only: the chunk alone and the decodes alone ----
+    parts = None
+    if varlen:
+        parts = varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak)
 
     if rank != 0:
         return
-    traffic = recorded_traffic()
-    achieved = attn_bytes / (t_attn * 1e-3) / 1e9
+    launches_per_step = 1 + (2 if not varlen else (4 if max_q_len >= 2 else 2))
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block permutation)",
-        "config": {"workload": "gqa_decode_128seq_llama70b_layer", "num_seqs": S, "num_heads": Hq,
-                   "num_kv_heads": b.num_kv_heads, "head_dim": d, "block_size": 16,
-                   "context_lens": f"uniform[500,2500] seed {args.seed}",
-                   "sum_context": int(b.context_lens.astype(np.int64).sum()),
-                   "num_blocks": b.num_blocks, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (512 MB write); KV pool 2x"
-                         f"{b.k_cache.nbytes / 1e6:.0f} MB > L2"},
-        "pct_of_peak": 100.0 * value / world / peak,
+        "metric": METRIC if args.config == "gqa_decode" else f"{name}: HBM GB/s of the step",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block permutation)",
+        "config": {"workload": name, **cfg, "seed": seed,
+                   "sum_context": int(b.context_lens.astype(np.int64).sum()), "num_blocks": b.num_blocks,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write); KV pool "
+                         f"2 x {b.k_cache.nbytes / 1e6:.0f} MB"},
+        "pct_of_peak": 100.0 * value / world / hbm_peak,
         "seq_steps_per_s": S * world / (t_step * 1e-3),
         "algorithmic_bytes_per_step": total_bytes,
         "kv_write_us": 1e3 * sum(kv_ms) / len(kv_ms),
         "attention_us": 1e3 * t_attn,
-        "e2e": {"value": total_bytes * world / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
-        "gpu_launches": 3 * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel + paged_decode_merge_kernel",
-                     "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} (hbm_gbs burst)",
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
-                     "algorithmic_bytes": attn_bytes},
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not varlen:
+        traffic = recorded_traffic("decode", DECODE_SOURCES)
+        achieved = attn_bytes / (t_attn * 1e-3) / 1e9
+        line["roofline"] = {
+            "bound": "hbm", "kernel": "paged_decode_kernel (+ merge_parts_kernel, timed together)",
+            "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+            "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+            "algorithmic_bytes": attn_bytes}
+    else:
+        line.update(parts)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(b)
+        dt, share, cores = oracle_step_time(b, sample_seqs(b, 32))
+        line["cpu_baseline"] = {
+            "value": total_bytes * share / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {min(32, b.num_seqs)} of {b.num_seqs} sequences (all heads, KV write of "
+                      f"every new token), one step, bytes scaled by their share of the total context"}
     print(json.dumps(line), flush=True)
+
+
+def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak):
+    """Times the chunk rows alone and the decode rows alone (same pool, same call)."""
+    res = {}
+    ql = b.q_lens
+    groups = {"chunk": np.nonzero(ql >= 2)[0], "decodes": np.nonzero(ql == 1)[0]}
+    for key, seqs in groups.items():
+        if len(seqs) == 0:
+            continue
+        rows = np.concatenate([np.arange(b.query_start_loc[s], b.query_start_loc[s + 1]) for s in seqs])
+        qq = torch.from_numpy(b.q[rows].view(np.int16)).to(dev).view(torch.bfloat16)
+        qsl = torch.from_numpy(np.concatenate([[0], np.cumsum(ql[seqs])]).astype(np.int32)).to(dev)
+        tables = torch.from_numpy(np.ascontiguousarray(b.block_tables[seqs])).to(dev)
+        lens = torch.from_numpy(np.ascontiguousarray(b.context_lens[seqs])).to(dev)
+        o = torch.empty_like(qq)
+        ws = torch.empty(pkv.workspace_size(pkv.OP_VARLEN, len(seqs), qq.shape[0], b.num_heads,
+                                            b.num_kv_heads, b.head_dim), dtype=torch.uint8, device=dev)
+        mq = int(ql[seqs].max())
+
+        def call():
+            pkv.paged_attention_varlen(o, qq, qsl, kc, vc, tables, lens, b.scale, causal=b.causal,
+                                       max_q_len=mq, workspace=ws)
+        for _ in range(5):
+            call()
+        ts = []
+        for i in range(50):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        t = float(np.median(ts))
+        if key == "chunk":
+            fl = chunk_flops(b.context_lens[seqs], ql[seqs], b.head_dim, b.num_heads)
+            tf = fl / (t * 1e-3) / 1e12
+            res["chunk_us"] = t * 1e3
+            res["chunk_tflops"] = tf
+            res["roofline"] = {"bound": "tensor", "kernel": "paged_prefill_kernel (+ merge, timed together)",
+                               "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                               "peak_source": "measured bf16_tflops (burst cuBLAS)", "traffic": None,
+                               "algorithmic_flops": fl}
+        else:
+            byts = int(b.context_lens[seqs].astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 4
+            res["decodes_us"] = t * 1e3
+            res["decodes_gbs"] = byts / (t * 1e-3) / 1e9
+    return res
 
 
 if __name__ == "__main__":
