@@ -98,6 +98,24 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, in
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Tensor map over q [total_q][num_heads][head_dim] for the chunked-prefill tiles: one
+// box is `tokens` consecutive query rows x the `group` heads of one KV head x 64
+// columns, landing in shared memory as [token][head][64] (row = token * group + head),
+// 128-byte swizzled -- the K-major A operand of the tensor-core MMA.
+int encode_q_map(CUtensorMap *map, const void *q, int total_q, int num_heads, int head_dim,
+                 int group, int tokens) {
+    cuuint64_t dims[4] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)num_heads,
+                          (cuuint64_t)total_q};
+    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)group, (cuuint32_t)tokens};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // ---- decode planning -------------------------------------------------------
 struct DecodePlan {
     int group, warps_per_head, heads_per_cta, head_tiles, items, stage_bytes, num_stages, grid;
@@ -333,8 +351,10 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
                     scale, ws, p.bytes, *d, p, s);
     if (st != PKV_OK || !prefill_rows) return st;
     // Multi-token rows (prefill chunks): the chunked-prefill kernel.
-    CUtensorMap kmap, vmap;
-    st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_q_map(&qmap, q, total_q_tokens, num_heads, head_dim, pp.group, pp.tokens_per_tile);
+    if (st == PKV_OK)
+        st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
     if (st == PKV_OK)
         st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
     if (st != PKV_OK) return st;
@@ -362,7 +382,7 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     a.ws_o = reinterpret_cast<float *>(pws + pp.off_o);
     a.max_seqs = num_seqs;
     a.err = d->err;
-    return pkv::launch_paged_prefill(head_dim, kmap, vmap, a, pp, s) == cudaSuccess ? PKV_OK
+    return pkv::launch_paged_prefill(head_dim, qmap, kmap, vmap, a, pp, s) == cudaSuccess ? PKV_OK
                                                                                    : PKV_ERR_CUDA;
 }
 

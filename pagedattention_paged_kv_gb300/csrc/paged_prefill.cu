@@ -26,6 +26,7 @@
 #include "merge.cuh"
 #include "paged_prefill.cuh"
 #include "pkv_split.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -201,45 +202,92 @@ __device__ void write_jobs_and_invalid_rows(const PrefillArgs &a, const int64_t 
     }
 }
 
+// Layout of the kernel's shared memory (offsets from a 1024-byte-aligned base).
 template <int D>
-__global__ void __launch_bounds__(288, 1)
-paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
+struct PrefillSmem {
+    static constexpr int KT = 64;                              // keys per chunk
+    static constexpr int BPC = KT / kBS;                       // blocks per chunk
+    static constexpr uint32_t Q_DC = 128 * 128;                // one 64-column chunk of Q (128 rows)
+    static constexpr uint32_t Q_BYTES = (D / 64) * Q_DC;       // Q tile
+    static constexpr uint32_t P_BYTES = 128 * KT * 2;          // P of one chunk, 128 rows
+    static constexpr uint32_t KV_DC = KT * 128;                // 64 keys x 64 columns
+    static constexpr uint32_t STG = (D / 64) * KV_DC;          // K or V of one chunk
+    static constexpr uint32_t OFF_P = Q_BYTES;
+    static constexpr uint32_t OFF_STAGES = OFF_P + 2 * P_BYTES;
+    static constexpr uint32_t TMEM_COLS = 256;                 // S[2] (2 x 64) + O (<= 128)
+    static constexpr uint32_t COL_O = 128;
+};
+
+// The CTA's share is walked segment by segment (a segment = the part of one tile that
+// lies in the share); each segment's blocks go in chunks of up to 4 (64 keys).
+struct Segment {
+    UnitPos u;
+    int64_t end;     // one past the segment's last unit
+    int nblk;        // blocks in the segment
+    int chunks;      // ceil(nblk / 4)
+};
+
+__device__ __forceinline__ void segment_at(const PrefillArgs &a, const int64_t *pre, int64_t f,
+                                           int64_t hi, Segment &sg) {
+    locate(a, pre, f, sg.u);
+    sg.end = min64(hi, sg.u.tile_begin + sg.u.tile_blocks);
+    sg.nblk = (int)(sg.end - f);
+    sg.chunks = (sg.nblk + 3) / 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+                     const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
-    constexpr int KSTEPS = D / 16;
-    constexpr int NT_D = D / 8;
+    using L = PrefillSmem<D>;
     constexpr int DCH = D / 64;
-    constexpr uint32_t kStageBytes = kBS * D * 2;
+    constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, L::KT, 0, 0);
+    constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, D, 0, 1);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = a.num_stages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * kStageBytes);
-    uint64_t *empty = full + NST;
-    int64_t *scan_tmp = reinterpret_cast<int64_t *>(empty + NST);  // 32 entries
-    volatile int *abort_flag = reinterpret_cast<int *>(scan_tmp + 32);
-    int64_t *pre = scan_tmp + 34;
+    uint8_t *sQ = smem, *sP = smem + L::OFF_P, *sStage = smem + L::OFF_STAGES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)NST * L::STG);
+    uint64_t *q_full = bars, *q_empty = bars + 1, *s_full = bars + 2, *p_full = bars + 4,
+             *pv_done = bars + 6, *o_free = bars + 8, *mma_done = bars + 9;
+    uint64_t *kv_full = bars + 10, *kv_empty = kv_full + NST;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(kv_empty + NST);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int64_t *scan_tmp = reinterpret_cast<int64_t *>(tmem_slot + 2);  // 32 entries
+    int64_t *pre = scan_tmp + 32;
 
-    const int group = a.group, TPT = a.tokens_per_tile;
-    const int rows = TPT * group;
-    const int ncw = (rows + 15) / 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = a.group, TPT = a.tokens_per_tile;
+    const int tile_rows = TPT * group;
 
     if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&pv_done[i], 1);
+        }
+        mbar_init(o_free, 128);
+        mbar_init(mma_done, 1);
         for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], ncw);
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x == 32 * ncw) {
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&q_map);
         tma_prefetch_desc(&k_map);
         tma_prefetch_desc(&v_map);
     }
     pdl_wait();
     pdl_trigger();
-    build_seq_prefix(a, pre, scan_tmp);
+    build_seq_prefix(a, pre, scan_tmp);  // ends with __syncthreads
     const int64_t T = pre[a.num_seqs];
     const int ge = split_ctas(T, a.grid, 4);
     if (blockIdx.x == 0) write_jobs_and_invalid_rows<D>(a, pre, T, ge);
@@ -247,186 +295,297 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap k_map,
     const int c = blockIdx.x;
     const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
 
-    if (warp == ncw) {
-        // ------------------------------ producer ------------------------------
+    if (warp == 1) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
         const uint64_t policy = l2_policy_evict_normal();
-        uint32_t stage = 0, phase = 0, issued = 0;
+        uint32_t fill = 0;
+        int seg_i = 0;
         bool ok = true;
-        for (int64_t f0 = lo; f0 < hi && ok; f0 += 32) {
-            const int64_t f = f0 + lane;
-            int bid = -1, kvh = 0;
-            if (f < hi) {
-                UnitPos u;
-                locate(a, pre, f, u);
-                kvh = u.kvh;
-                bid = a.block_tables[(int64_t)u.s * a.max_blocks_per_seq + u.kb];
-                if (bid < 0 || (int64_t)bid >= a.num_blocks) {
-                    flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    bid = -1;
+        for (int64_t f = lo; f < hi && ok;) {
+            Segment sg;
+            segment_at(a, pre, f, hi, sg);
+            const UnitPos &u = sg.u;
+            if (lane == 0) {
+                if (seg_i > 0) ok = mbar_wait(q_empty, (seg_i - 1) & 1, abort_flag);
+                if (ok) {
+                    mbar_arrive_expect_tx(q_full, DCH * tile_rows * 128);
+                    for (int dc = 0; dc < DCH; ++dc)
+                        tma_load_4d(sQ + dc * L::Q_DC, &q_map, q_full, 0, dc, u.kvh * group,
+                                    (int)(u.t.q_row0 + u.qt * TPT), policy);
                 }
             }
-            const int n = (int)min64(32, hi - f0);
-            for (int j = 0; j < n; ++j) {
-                const int b = __shfl_sync(0xffffffffu, bid, j);
-                const int h = __shfl_sync(0xffffffffu, kvh, j);
-                if (lane == 0) {
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                        uint8_t *dst = smem + (size_t)stage * kStageBytes;
-                        const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
-#pragma unroll
-                        for (int dc = 0; dc < DCH; ++dc)
-                            tma_load_5d(dst + dc * (kBS * 128), map, &full[stage], 0, 0, h, dc,
-                                        b, policy);
-                        ++issued;
-                        if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const int64_t trow = (int64_t)u.s * a.max_blocks_per_seq + u.kb;
+            for (int b0 = 0; b0 < sg.nblk && ok; b0 += 32) {
+                int bid = -1;
+                if (b0 + lane < sg.nblk) {
+                    bid = a.block_tables[trow + b0 + lane];
+                    if (bid < 0 || (int64_t)bid >= a.num_blocks) {
+                        flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        bid = -1;  // TMA fills an out-of-range box with zeros
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                const int n32 = min(32, sg.nblk - b0);
+                for (int cb = 0; cb < n32 && ok; cb += L::BPC) {
+                    int ids[L::BPC];
+#pragma unroll
+                    for (int i = 0; i < L::BPC; ++i) {
+                        const int v = __shfl_sync(0xffffffffu, bid, (cb + i) & 31);
+                        ids[i] = cb + i < n32 ? v : -1;  // missing blocks load as zeros
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kv = 0; kv < 2; ++kv) {
+                            const uint32_t st = fill % NST, round = fill / NST;
+                            if (!mbar_wait(&kv_empty[st], (round & 1) ^ 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&kv_full[st], L::STG);
+                            uint8_t *dst = sStage + (size_t)st * L::STG;
+                            const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
+#pragma unroll
+                            for (int i = 0; i < L::BPC; ++i)
+#pragma unroll
+                                for (int dc = 0; dc < DCH; ++dc)
+                                    tma_load_5d(dst + dc * L::KV_DC + i * (kBS * 128), map, &kv_full[st],
+                                                0, 0, u.kvh, dc, ids[i], policy);
+                            ++fill;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
             }
+            f = sg.end;
+            ++seg_i;
         }
         if (!ok && lane == 0) {
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
             *abort_flag = 1;
-            const uint32_t pending = minu32(issued, (uint32_t)NST);
-            uint32_t st = stage, ph = phase;
-            for (uint32_t i = 0; i < pending; ++i) {
-                if (st == 0) { st = NST; ph ^= 1; }
-                --st;
-                mbar_wait(&full[st], ph, nullptr);
-            }
+            // let issued copies land before shared memory is released
+            const uint32_t pending = minu32(fill, (uint32_t)NST);
+            for (uint32_t k = fill - pending; k < fill; ++k)
+                mbar_wait(&kv_full[k % NST], (k / NST) & 1, nullptr);
+            if (seg_i > 0) mbar_wait(q_full, (seg_i - 1) & 1, nullptr);
         }
-        return;
-    }
-    if (warp > ncw) return;
-
-    // -------------------------------- consumers --------------------------------
-    const int g_row = lane >> 2, q4 = lane & 3;
-    const int ra = warp * 16 + g_row, rb = ra + 8;  // this lane's two tile rows
-    const uint32_t smem_base = smem_u32(smem);
-    const float sl2 = a.scale_log2;
-    uint32_t stage = 0, phase = 0;
-    int64_t f = lo;
-    RowState<D> st;
-    while (f < hi) {
-        UnitPos u;
-        locate(a, pre, f, u);
-        const int64_t tile_end = u.tile_begin + u.tile_blocks;
-        const int64_t seg_end = min64(hi, tile_end);
-        const int tile_tokens = (int)min64(TPT, u.t.q_len - u.qt * TPT);
-        const int tok_a = ra / group, tok_b = rb / group;
-        const bool va = ra < rows && tok_a < tile_tokens;
-        const bool vb = rb < rows && tok_b < tile_tokens;
-        const int64_t first_pos = (int64_t)(u.t.ctx - u.t.q_len) + u.qt * TPT;
-        const int ctx = u.t.ctx;
-        // keys a row may see: [0, lim)
-        const int64_t lim_a = a.causal ? min64(first_pos + min(tok_a, tile_tokens - 1) + 1, ctx) : ctx;
-        const int64_t lim_b = a.causal ? min64(first_pos + min(tok_b, tile_tokens - 1) + 1, ctx) : ctx;
-        // keys every row of the warp may see (for the no-mask fast path)
-        const int64_t lim_warp = a.causal
-            ? min64(first_pos + min((warp * 16) / group, tile_tokens - 1) + 1, ctx) : ctx;
-
-        uint32_t qa[KSTEPS][4];
-        {
-            const int64_t qrow_a = u.t.q_row0 + u.qt * TPT + tok_a;
-            const int64_t qrow_b = u.t.q_row0 + u.qt * TPT + tok_b;
-            const uint32_t *pa = reinterpret_cast<const uint32_t *>(
-                a.q + (qrow_a * a.num_heads + (int64_t)u.kvh * group + ra % group) * D);
-            const uint32_t *pb = reinterpret_cast<const uint32_t *>(
-                a.q + (qrow_b * a.num_heads + (int64_t)u.kvh * group + rb % group) * D);
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            const uint32_t tS = tmem, tO = tmem + L::COL_O;
+            uint32_t g = 0;
+            int seg_i = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t gp, bool first) -> bool {
+                if (first && seg_i > 0 && !mbar_wait(o_free, (seg_i - 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(&p_full[gp & 1], (gp >> 1) & 1, abort_flag)) return false;
+                const uint32_t vf = 2 * gp + 1;
+                if (!mbar_wait(&kv_full[vf % NST], (vf / NST) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t pa = smem_u32(sP + (gp & 1) * L::P_BYTES);
+                const uint32_t va = smem_u32(sStage + (size_t)(vf % NST) * L::STG);
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                const int col = ks * 16 + 2 * q4;
-                qa[ks][0] = va ? __ldg(pa + col / 2) : 0u;
-                qa[ks][1] = vb ? __ldg(pb + col / 2) : 0u;
-                qa[ks][2] = va ? __ldg(pa + (col + 8) / 2) : 0u;
-                qa[ks][3] = vb ? __ldg(pb + (col + 8) / 2) : 0u;
-            }
-        }
-        st.reset();
-
-        bool ok = true;
-        for (; f < seg_end; ++f) {
-            const int64_t key0 = (f - u.tile_begin) * kBS;
-            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            float sacc[2][4];
-            qk_block<D>(sacc, qa, smem_base + stage * kStageBytes, kBS * 128, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-
-            if (key0 + kBS <= lim_warp) {  // the whole block is visible to every row
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sacc[0][i] *= sl2;
-                    sacc[1][i] *= sl2;
-                }
-            } else {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int64_t key = key0 + nt * 8 + 2 * q4 + e;
-                        sacc[nt][e] = key < lim_a ? sacc[nt][e] * sl2 : -INFINITY;
-                        sacc[nt][2 + e] = key < lim_b ? sacc[nt][2 + e] * sl2 : -INFINITY;
+                for (int ks = 0; ks < L::KT / 16; ++ks)
+                    umma_bf16(tO, umma_desc_sw128(pa + ks * 32, 16, 1024),
+                              umma_desc_sw128(va + ks * 2048, L::KV_DC, 1024), IDESC_PV,
+                              !(first && ks == 0));
+                umma_commit(&pv_done[gp & 1]);
+                umma_commit(&kv_empty[vf % NST]);
+                return true;
+            };
+            for (int64_t f = lo; f < hi && ok;) {
+                Segment sg;
+                segment_at(a, pre, f, hi, sg);
+                ok = mbar_wait(q_full, seg_i & 1, abort_flag);
+                tc_fence_after();
+                const uint32_t qa = smem_u32(sQ);
+                for (int ch = 0; ch < sg.chunks && ok; ++ch, ++g) {
+                    if (g >= 2 && !mbar_wait(&p_full[g & 1], ((g - 2) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t kf = 2 * g;
+                    if (!mbar_wait(&kv_full[kf % NST], (kf / NST) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ka = smem_u32(sStage + (size_t)(kf % NST) * L::STG);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t dc = ks / 4, ko = (ks % 4) * 32;
+                        umma_bf16(tS + (g & 1) * L::KT, umma_desc_sw128(qa + dc * L::Q_DC + ko, 16, 1024),
+                                  umma_desc_sw128(ka + dc * L::KV_DC + ko, 16, 1024), IDESC_QK, ks > 0);
+                    }
+                    umma_commit(&s_full[g & 1]);
+                    umma_commit(&kv_empty[kf % NST]);
+                    if (ch == sg.chunks - 1) umma_commit(q_empty);
+                    if (ch >= 1 && !issue_pv(g - 1, ch == 1)) ok = false;
+                }
+                if (ok && !issue_pv(g - 1, sg.chunks == 1)) ok = false;
+                f = sg.end;
+                ++seg_i;
             }
-            uint32_t pa[4];
-            softmax_update<D>(st, sacc, pa);
-
-            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            if (key0 + kBS <= ctx)
-                pv_block<D, false>(st, pa, smem_base + stage * kStageBytes, kBS * 128, kBS, lane);
-            else
-                pv_block<D, true>(st, pa, smem_base + stage * kStageBytes, kBS * 128,
-                                  (int)(ctx - key0), lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
+            if (!ok) {
+                flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA this thread issued is finished before TMEM is released
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ----------------------- softmax (one thread per row) -----------------------
+        const int quarter = warp & 3;  // the TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + tl, tO = tmem + tl + L::COL_O;
+        const int tid = threadIdx.x - 64;  // 0..127
+        const float sl2 = a.scale_log2;
+        uint32_t g = 0;
+        int seg_i = 0;
+        bool ok = true;
+        for (int64_t f = lo; f < hi && ok;) {
+            Segment sg;
+            segment_at(a, pre, f, hi, sg);
+            const UnitPos &u = sg.u;
+            const int ctx = u.t.ctx;
+            const int tile_tokens = (int)min64(TPT, u.t.q_len - u.qt * TPT);
+            const int tok = row / group, hg = row - tok * group;
+            const bool rvalid = row < tile_rows && tok < tile_tokens;
+            const int64_t first_pos = (int64_t)(ctx - u.t.q_len) + u.qt * TPT;
+            const int64_t lim = a.causal ? min64(first_pos + min(tok, tile_tokens - 1) + 1, ctx) : ctx;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int ch = 0; ch < sg.chunks; ++ch, ++g) {
+                const int nb = min(L::BPC, sg.nblk - L::BPC * ch);
+                const int64_t key0 = (u.kb + (int64_t)L::BPC * ch) * kBS;
+                const int nkeys = nb * kBS;
+                if (!mbar_wait(&s_full[g & 1], (g >> 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[2][32];
+                tmem_ld32(tS + (g & 1) * L::KT, sr[0]);
+                tmem_ld32(tS + (g & 1) * L::KT + 32, sr[1]);
+                tmem_wait_ld();
+                // visible keys of this chunk for this row: [0, vis)
+                const int vis = (int)max64(0, min64(lim - key0, (int64_t)nkeys));
+                float sv[64];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float x = __uint_as_float(sr[j >> 5][j & 31]) * sl2;
+                    sv[j] = j < vis ? x : -INFINITY;
+                    mx = fmaxf(mx, sv[j]);
+                }
+                const bool up = mx > m_ref + kRescaleSlack;
+                if (__any_sync(0xffffffffu, up)) {
+                    const float alpha = up ? fast_exp2(m_ref - mx) : 1.f;
+                    if (ch > 0) {
+                        // O holds this segment's earlier chunks: wait for the last PV, rescale.
+                        const uint32_t gp = g - 1;
+                        if (!mbar_wait(&pv_done[gp & 1], (gp >> 1) & 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int q = 0; q < D / 32; ++q) {
+                            uint32_t r[32];
+                            tmem_ld32(tO + q * 32, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                            tmem_st32(tO + q * 32, r);
+                        }
+                        tmem_wait_st();
+                    }
+                    l *= alpha;
+                    if (up) m_ref = mx;
+                }
+                const float base = m_ref == -INFINITY ? 0.f : m_ref;
+                uint32_t pk[32];
+                float ps = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    pk[j] = pack_bf16x2(fast_exp2(sv[2 * j] - base), fast_exp2(sv[2 * j + 1] - base));
+                    ps += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+                }
+                l += ps;
+                // P buffer g & 1 is free once PV(g - 2) has read it
+                if (g >= 2 && !mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+                uint8_t *prow = sP + (g & 1) * L::P_BYTES + row * 128;
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16)
+                    *reinterpret_cast<uint4 *>(prow + ((c16 ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+                if (key0 + nkeys > ctx) {
+                    // The chunk runs past the context: the pool rows there may hold NaN, and
+                    // 0 * NaN would poison O, so zero those V rows before PV reads them.
+                    const uint32_t vf = 2 * g + 1;
+                    if (!mbar_wait(&kv_full[vf % NST], (vf / NST) & 1, abort_flag)) { ok = false; break; }
+                    uint8_t *vst = sStage + (size_t)(vf % NST) * L::STG;
+                    const int r0 = (int)(ctx - key0), nrows = nkeys - r0;
+                    for (int i = tid; i < nrows * DCH * 8; i += 128) {
+                        const int rr = r0 + i / (DCH * 8), rem = i % (DCH * 8);
+                        *reinterpret_cast<uint4 *>(vst + (rem >> 3) * L::KV_DC + rr * 128 + ((rem & 7) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&p_full[g & 1]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l for the tile, or the part for the merge ----
+            const uint32_t gl = g - 1;
+            if (!mbar_wait(&pv_done[gl & 1], (gl >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const bool whole = lo <= u.tile_begin && sg.end == u.tile_begin + u.tile_blocks;
+            const float inv = 1.f / l;
+            const int64_t qrow = u.t.q_row0 + u.qt * TPT + tok;
+            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)u.kvh * group + hg) * D;
+            const int slot = whole ? 0 : part_slot(c, u.tile_begin, T, ge);
+            float *wrow = a.ws_o + ((int64_t)slot * tile_rows + row) * D;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t r[32];
+                tmem_ld32(tO + q * 32, r);
+                tmem_wait_ld();
+                if (!rvalid) continue;
+                if (whole) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + q * 32 + j) = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<uint4 *>(wrow + q * 32 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                }
+            }
+            if (!whole && rvalid) a.ws_ml[(int64_t)slot * tile_rows + row] = make_float2(m_ref, l);
+            tc_fence_before();
+            mbar_arrive(o_free);
+            f = sg.end;
+            ++seg_i;
         }
         if (!ok) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
             *abort_flag = 1;
-            return;
         }
-
-        finish_sums<D>(st);
-        const bool whole = lo <= u.tile_begin && seg_end == tile_end;
-        if (whole) {
-            const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
-            const int64_t qrow_a = u.t.q_row0 + u.qt * TPT + tok_a;
-            const int64_t qrow_b = u.t.q_row0 + u.qt * TPT + tok_b;
-            __nv_bfloat16 *oa = a.out + (qrow_a * a.num_heads + (int64_t)u.kvh * group + ra % group) * D;
-            __nv_bfloat16 *ob = a.out + (qrow_b * a.num_heads + (int64_t)u.kvh * group + rb % group) * D;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (va) *reinterpret_cast<uint32_t *>(oa + col) = pack_bf16x2(st.o[n][0] * inv0, st.o[n][1] * inv0);
-                if (vb) *reinterpret_cast<uint32_t *>(ob + col) = pack_bf16x2(st.o[n][2] * inv1, st.o[n][3] * inv1);
-            }
-        } else {
-            const int slot = part_slot(c, u.tile_begin, T, ge);
-            float *ws = a.ws_o + (int64_t)slot * rows * D;
-            float2 *ml = a.ws_ml + (int64_t)slot * rows;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (va) *reinterpret_cast<float2 *>(ws + (int64_t)ra * D + col) = make_float2(st.o[n][0], st.o[n][1]);
-                if (vb) *reinterpret_cast<float2 *>(ws + (int64_t)rb * D + col) = make_float2(st.o[n][2], st.o[n][3]);
-            }
-            if (q4 == 0) {
-                if (va) ml[ra] = make_float2(st.m0, st.l0);
-                if (vb) ml[rb] = make_float2(st.m1, st.l1);
-            }
-        }
-        f = seg_end;
     }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -436,15 +595,16 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     if (num_kv_heads <= 0 || num_heads % num_kv_heads) return PKV_ERR_UNSUPPORTED;
     p->group = num_heads / num_kv_heads;
     if (p->group > 8) return PKV_ERR_UNSUPPORTED;
-    p->tokens_per_tile = 16 * (8 / p->group);
-    p->rows = p->tokens_per_tile * p->group;
-    p->warps = (p->rows + 15) / 16;
+    p->tokens_per_tile = 16 * (8 / p->group);  // 128 / group rounded down to 16 tokens
+    p->rows = p->tokens_per_tile * p->group;    // <= 128 = the MMA's M
+    p->warps = 6;
     p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
-    p->stage_bytes = kBS * head_dim * 2;
-    const size_t fixed = 1024 + 34 * 8 + 8 * (size_t)(num_seqs + 1) + 8;
+    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 128 * 128, p_bytes = 2 * 128 * 64 * 2;
+    p->stage_bytes = 64 * head_dim * 2;
+    const size_t fixed = 1024 + q_bytes + p_bytes + 8 * 10 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
     int nst = (int)(((int64_t)smem_optin - (int64_t)fixed) / (p->stage_bytes + 16));
-    if (nst > 32) nst = 32;
+    if (nst > 8) nst = 8;
     if (nst < 4) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
     p->smem = fixed + (size_t)nst * (p->stage_bytes + 16);
@@ -457,12 +617,13 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
 }
 
 template <int D>
-static cudaError_t launch_prefill_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
-                                    const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream) {
+static cudaError_t launch_prefill_d(const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                    const CUtensorMap &v_map, const PrefillArgs &a,
+                                    const PrefillPlan &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(paged_prefill_kernel<D>, dim3(a.grid), dim3((p.warps + 1) * 32), p.smem, stream,
+    e = launch_pdl(paged_prefill_kernel<D>, dim3(a.grid), dim3(p.warps * 32), p.smem, stream, q_map,
                    k_map, v_map, a);
     if (e != cudaSuccess) return e;
     MergeArgs m;
@@ -475,10 +636,11 @@ static cudaError_t launch_prefill_d(const CUtensorMap &k_map, const CUtensorMap 
     return launch_merge<D>(m, a.grid, stream);
 }
 
-cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
-                                 const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream) {
-    return head_dim == 128 ? launch_prefill_d<128>(k_map, v_map, a, p, stream)
-                           : launch_prefill_d<64>(k_map, v_map, a, p, stream);
+cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                 const CUtensorMap &v_map, const PrefillArgs &a,
+                                 const PrefillPlan &p, cudaStream_t stream) {
+    return head_dim == 128 ? launch_prefill_d<128>(q_map, k_map, v_map, a, p, stream)
+                           : launch_prefill_d<64>(q_map, k_map, v_map, a, p, stream);
 }
 
 }  // namespace pkv

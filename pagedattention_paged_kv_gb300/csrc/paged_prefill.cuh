@@ -45,7 +45,8 @@ struct PrefillPlan {
 // PKV_ERR_UNSUPPORTED.
 int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
                  int smem_optin, PrefillPlan *p);
-cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
-                                 const PrefillArgs &a, const PrefillPlan &p, cudaStream_t stream);
+cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                 const CUtensorMap &v_map, const PrefillArgs &a,
+                                 const PrefillPlan &p, cudaStream_t stream);
 
 }  // namespace pkv
