@@ -1,0 +1,220 @@
+"""Iteration-level (continuous-batching) scheduler over the paged KV pool (host).
+
+Follows the loop that the pages print:
+
+* "Servis Motor İçleri: PagedAttention, Sürekli Batching, parçalanmış Prefill"
+  (aiengineeringfromscratch.com, Phase 17 - 04), "What the scheduler looks like":
+  every iteration (1) drops finished sequences and returns their blocks, (2) admits
+  sequences from the head of the waiting queue while there are free blocks for them,
+  (3) gives every running sequence either its next prefill chunk (up to 512 tokens,
+  "Chunked prefill protects the TTFT tail") or one decode token, and (4) runs one
+  fused forward over that batch.
+* "vLLM推理引擎架构PagedAttention机制与高吞吐推理" (lpnh.cn) §3.1 Scheduler: admission
+  allocates ceil(prompt_len / block_size) blocks (a failed allocation puts the
+  sequence back at the head of the queue and stops admission); a running sequence that
+  grows past its blocks gets one more block, and if none is free it is preempted:
+  its blocks are freed, its computed tokens reset to 0 and it goes to the tail of the
+  waiting queue (§3.2: recovery by recomputation, not swapping).
+
+Readings where the pages leave a step open (see the design notes): a sequence finishes
+when it has produced output_len tokens, one per decode step; the last prefill chunk
+produces no token; a preempted sequence recomputes its prompt and the tokens it had
+already produced as one longer prefill; the waiting queue is FIFO; running sequences
+keep their admission order in the batch.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import BLOCK_SIZE, BlockManager, OutOfBlocks
+
+
+@dataclass
+class Sequence:
+    seq_id: int
+    prompt_len: int
+    output_len: int
+    arrival: int = 0
+    block_table: list = field(default_factory=list)
+    prefill_target: int = 0   # tokens to (re)compute before decoding: prompt (+ output so far)
+    computed: int = 0         # tokens whose K/V are in the cache
+    decoded: int = 0          # output tokens produced
+    preemptions: int = 0
+
+    def __post_init__(self):
+        if self.prefill_target == 0:
+            self.prefill_target = self.prompt_len
+
+    @property
+    def in_prefill(self) -> bool:
+        return self.computed < self.prefill_target
+
+    @property
+    def finished(self) -> bool:
+        return self.decoded >= self.output_len
+
+
+@dataclass
+class ScheduledItem:
+    seq: Sequence
+    start: int       # first position written this iteration
+    q_len: int       # tokens written and attended this iteration
+
+    @property
+    def context_len(self) -> int:
+        return self.start + self.q_len
+
+
+@dataclass
+class IterationBatch:
+    """The metadata of one fused attention call (host arrays)."""
+    items: list
+    query_start_loc: np.ndarray   # int32 [S+1]
+    context_lens: np.ndarray      # int32 [S]
+    block_tables: np.ndarray      # int32 [S, MB], unused entries -1
+    token_seq: np.ndarray         # int32 [T] batch row of each new token
+    token_pos: np.ndarray         # int32 [T] absolute position of each new token
+    admitted: int = 0
+    finished: int = 0
+    preempted: int = 0
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.items)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1]) if len(self.query_start_loc) else 0
+
+    @property
+    def max_q_len(self) -> int:
+        return max((it.q_len for it in self.items), default=0)
+
+
+class Scheduler:
+    def __init__(self, block_manager: BlockManager, max_num_seqs: int = 128, chunk_size: int = 512,
+                 block_size: int = BLOCK_SIZE, max_num_batched_tokens: int | None = None):
+        self.bm = block_manager
+        self.max_num_seqs = int(max_num_seqs)
+        self.chunk_size = int(chunk_size)
+        self.block_size = int(block_size)
+        self.max_num_batched_tokens = max_num_batched_tokens
+        self.waiting: list[Sequence] = []
+        self.running: list[Sequence] = []
+        self.done: list[Sequence] = []
+        self.iteration = 0
+        self.total_preemptions = 0
+
+    # -- queue -------------------------------------------------------------------
+    def add(self, seq: Sequence) -> None:
+        self.waiting.append(seq)
+
+    def _blocks_for(self, tokens: int) -> int:
+        return -(-tokens // self.block_size)
+
+    def _preempt(self, seq: Sequence) -> None:
+        """Free everything the sequence holds; it recomputes its tokens later."""
+        self.bm.free(seq.block_table)
+        seq.block_table = []
+        seq.prefill_target = seq.prompt_len + seq.decoded
+        seq.computed = 0
+        seq.preemptions += 1
+        self.total_preemptions += 1
+        self.waiting.append(seq)
+
+    # -- one iteration -------------------------------------------------------------
+    def schedule(self) -> IterationBatch:
+        finished = preempted = admitted = 0
+        # (1) release finished sequences
+        keep = []
+        for s in self.running:
+            if s.finished:
+                self.bm.free(s.block_table)
+                s.block_table = []
+                self.done.append(s)
+                finished += 1
+            else:
+                keep.append(s)
+        self.running = keep
+        # (2) growth: a decode step writing position p needs block p // block_size
+        keep = []
+        for s in self.running:
+            if not s.in_prefill:
+                pos = s.computed
+                need = self._blocks_for(pos + 1) - len(s.block_table)
+                if need > 0:
+                    try:
+                        s.block_table.extend(self.bm.allocate(need))
+                    except OutOfBlocks:
+                        self._preempt(s)
+                        preempted += 1
+                        continue
+            keep.append(s)
+        self.running = keep
+        # (3) admission from the head of the waiting queue
+        while self.waiting and len(self.running) < self.max_num_seqs:
+            s = self.waiting[0]
+            try:
+                s.block_table = self.bm.allocate(self._blocks_for(s.prefill_target))
+            except OutOfBlocks:
+                break
+            self.waiting.pop(0)
+            self.running.append(s)
+            admitted += 1
+        # (4) one chunk or one decode token per running sequence
+        items = []
+        budget = self.max_num_batched_tokens
+        for s in self.running:
+            if s.in_prefill:
+                n = min(self.chunk_size, s.prefill_target - s.computed)
+                if budget is not None:
+                    n = min(n, budget)
+                    if n <= 0:
+                        continue
+            else:
+                n = 1
+                if budget is not None and budget < 1:
+                    continue
+            items.append(ScheduledItem(s, s.computed, n))
+            if budget is not None:
+                budget -= n
+        self.iteration += 1
+        return self._pack(items, admitted, finished, preempted)
+
+    def complete(self, batch: IterationBatch) -> None:
+        """Account for the forward pass of `batch`: cache grows, decodes emit tokens."""
+        for it in batch.items:
+            s = it.seq
+            was_decode = not s.in_prefill
+            s.computed += it.q_len
+            if was_decode:
+                s.decoded += 1
+
+    def _pack(self, items, admitted, finished, preempted) -> IterationBatch:
+        S = len(items)
+        q_lens = np.array([it.q_len for it in items], dtype=np.int32)
+        qsl = np.zeros(S + 1, dtype=np.int32)
+        if S:
+            np.cumsum(q_lens, out=qsl[1:])
+        ctx = np.array([it.context_len for it in items], dtype=np.int32)
+        mb = max((len(it.seq.block_table) for it in items), default=1)
+        tables = np.full((S, max(mb, 1)), -1, dtype=np.int32)
+        for i, it in enumerate(items):
+            tables[i, :len(it.seq.block_table)] = it.seq.block_table
+        tok_seq = np.repeat(np.arange(S, dtype=np.int32), q_lens)
+        tok_pos = (np.concatenate([np.arange(it.start, it.start + it.q_len, dtype=np.int32) for it in items])
+                   if S else np.zeros(0, np.int32))
+        return IterationBatch(items, qsl, ctx, tables, tok_seq, tok_pos, admitted, finished, preempted)
+
+    # -- accounting ----------------------------------------------------------------
+    def blocks_in_use(self) -> int:
+        return sum(len(s.block_table) for s in self.running)
+
+    def slot_waste(self) -> list:
+        """Per running sequence: slots its blocks hold beyond the tokens they are held
+        for (the prompt still being prefilled, else the tokens in the cache).  Measured
+        after complete(), each is at most block_size - 1."""
+        return [len(s.block_table) * self.block_size - (s.prefill_target if s.in_prefill else s.computed)
+                for s in self.running]
