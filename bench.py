@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--config", default="gqa_decode",
-                   choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen"])
+                   choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen", "cb_trace"])
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -307,11 +307,75 @@ class Packed:
         return self.dev[o:o + n].view(torch_dtype).view(shape)
 
 
+def run_trace(args, rank, world, local, dist):
+    """The continuous-batching trace: 300 scheduler iterations, each timed on the device
+    (KV write + one varlen attention call); reports per-iteration time and the
+    aggregate bytes/FLOPs of the whole trace."""
+    import torch
+    from pagedattention_paged_kv_gb300 import workloads as W
+    from pagedattention_paged_kv_gb300.engine import PagedKVEngine
+    from pagedattention_paged_kv_gb300.scheduler import Sequence
+    torch.cuda.set_device(local)
+    seed = (args.seed if args.seed is not None else 5001) + rank
+    NB, Hq, Hkv, d, iters = 65536, 64, 8, 128, 300
+    eng = PagedKVEngine(NB, Hq, Hkv, d, max_num_seqs=128, chunk_size=512, device=f"cuda:{local}")
+    by_iter = {}
+    for r in W.request_stream(seed=seed, iterations=iters):
+        by_iter.setdefault(r.arrival, []).append(r)
+    stream = torch.cuda.current_stream()
+    times, kvb, flops, seq_steps, tokens = [], 0, 0, 0, 0
+    with ClockSampler(local) as clk:
+        for it in range(iters):
+            for r in by_iter.get(it, []):
+                eng.add(Sequence(r.req_id, r.prompt_len, r.output_len, r.arrival))
+            batch = eng.schedule()
+            if batch.num_seqs:
+                q, k, v = W.iteration_values(seed, it, batch.num_tokens, Hq, Hkv, d)
+                qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+                kd = torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16)
+                vd = torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                eng.run(batch, qd, kd, vd)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+                ql = np.diff(batch.query_start_loc)
+                kvb += int(batch.context_lens[ql == 1].astype(np.int64).sum()) * Hkv * d * 4
+                flops += chunk_flops(batch.context_lens, ql, d, Hq)
+                seq_steps += int((ql == 1).sum())
+                tokens += batch.num_tokens
+            eng.complete(batch)
+    total_ms = max_over_ranks(sum(times), dist)
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": "continuous-batching trace: device time per iteration", "value": total_ms / len(times) * 1e3,
+        "unit": "us/iteration", "higher_is_better": False, "n_gpus": world, "steps": len(times), "warmup": 0,
+        "ms_per_step": total_ms / len(times), "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded request stream and N(0,1) bf16 values)",
+        "config": {"workload": "cb_trace_300_iterations", "arrivals": "Poisson(4) per iteration",
+                   "prompt": "log-normal mean 1500 std 600, cap 8192", "output": "uniform[16,512]",
+                   "max_running": 128, "chunk": 512, "num_blocks": NB, "num_heads": Hq, "num_kv_heads": Hkv,
+                   "head_dim": d, "seed": seed},
+        "total_ms": total_ms, "decode_kv_gbs": kvb / (total_ms * 1e-3) / 1e9,
+        "chunk_tflops_over_total_time": flops / (total_ms * 1e-3) / 1e12,
+        "decode_seq_steps_per_s": seq_steps / (total_ms * 1e-3), "tokens": tokens,
+        "p50_us": float(np.percentile(times, 50)) * 1e3, "p99_us": float(np.percentile(times, 99)) * 1e3,
+        "preemptions": eng.sched.total_preemptions, "finished": len(eng.sched.done),
+        "gpu_launches": 5 * len(times), "clocks": clk.summary(),
+    }), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local, dist = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.config == "cb_trace":
+        run_trace(args, rank, world, local, dist)
         return
     import torch
     import pagedattention_paged_kv_gb300 as pkv

@@ -352,7 +352,8 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     if (st != PKV_OK || !prefill_rows) return st;
     // Multi-token rows (prefill chunks): the chunked-prefill kernel.
     CUtensorMap qmap, kmap, vmap;
-    st = encode_q_map(&qmap, q, total_q_tokens, num_heads, head_dim, pp.group, pp.tokens_per_tile);
+    // one box per tile half
+    st = encode_q_map(&qmap, q, total_q_tokens, num_heads, head_dim, pp.group, pp.tokens_per_tile / 2);
     if (st == PKV_OK)
         st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
     if (st == PKV_OK)

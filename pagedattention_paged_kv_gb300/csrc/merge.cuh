@@ -37,8 +37,7 @@ struct MergeArgs {
     int num_heads;
 };
 
-constexpr int kMergeRowSplit = 4;    // CTAs per job (row slices)
-constexpr int kMergeMaxRows = 32;    // rows per CTA: ceil(slot_rows / kMergeRowSplit)
+constexpr int kMergeMaxRows = 32;    // rows per CTA; a job gets ceil(slot_rows / 32) CTAs
 constexpr int kMergeSmemParts = 32;  // parts whose (m, l) and weight stay in shared memory
 
 __device__ __forceinline__ void no_job(MergeJob &j) {
@@ -56,18 +55,18 @@ __global__ void __launch_bounds__(256) merge_parts_kernel(const MergeArgs m) {
     if (j.c0 < 0) return;
     const int nparts = j.c1 - j.c0 + 1;
     const int np_s = nparts < kMergeSmemParts ? nparts : kMergeSmemParts;
-    const int y = blockIdx.y;
-    const int my_rows = (j.rows - y + kMergeRowSplit - 1) / kMergeRowSplit;
+    const int y = blockIdx.y, ny = gridDim.y;  // rows y, y + ny, y + 2 ny, ...
+    const int my_rows = (j.rows - y + ny - 1) / ny;
     if (my_rows <= 0) return;
     // (m, l) of my rows x the first parts, all loads in flight together
     for (int i = threadIdx.x; i < my_rows * np_s; i += blockDim.x) {
         const int k = i / np_s, p = i - k * np_s;
         const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
-        s_ml[k][p] = m.ws_ml[(int64_t)slot * m.slot_rows + y + k * kMergeRowSplit];
+        s_ml[k][p] = m.ws_ml[(int64_t)slot * m.slot_rows + y + k * ny];
     }
     __syncthreads();
     for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
-        const int row = y + k * kMergeRowSplit;
+        const int row = y + k * ny;
         float M = -INFINITY;
         for (int p = 0; p < nparts; ++p)
             M = fmaxf(M, p < np_s ? s_ml[k][p].x
@@ -90,7 +89,7 @@ __global__ void __launch_bounds__(256) merge_parts_kernel(const MergeArgs m) {
     constexpr int D4 = D / 4;
     for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
         const int k = task / D4, d4 = task - k * D4;
-        const int row = y + k * kMergeRowSplit;
+        const int row = y + k * ny;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
         for (int p = 0; p < nparts; ++p) {
@@ -116,7 +115,8 @@ __global__ void __launch_bounds__(256) merge_parts_kernel(const MergeArgs m) {
 
 template <int D>
 cudaError_t launch_merge(const MergeArgs &m, int grid, cudaStream_t stream) {
-    return launch_pdl(merge_parts_kernel<D>, dim3(grid, kMergeRowSplit), dim3(256), 0, stream, m);
+    const int ny = (m.slot_rows + kMergeMaxRows - 1) / kMergeMaxRows;
+    return launch_pdl(merge_parts_kernel<D>, dim3(grid, ny), dim3(256), 0, stream, m);
 }
 
 }  // namespace pkv

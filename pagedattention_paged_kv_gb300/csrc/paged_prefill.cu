@@ -202,19 +202,23 @@ __device__ void write_jobs_and_invalid_rows(const PrefillArgs &a, const int64_t 
     }
 }
 
-// Layout of the kernel's shared memory (offsets from a 1024-byte-aligned base).
+// Layout of the kernel's shared memory (offsets from a 1024-byte-aligned base).  A work
+// tile is two halves of up to 128 query rows (one tcgen05 MMA M each); both halves use
+// every K/V chunk the producer loads.
 template <int D>
 struct PrefillSmem {
     static constexpr int KT = 64;                              // keys per chunk
     static constexpr int BPC = KT / kBS;                       // blocks per chunk
-    static constexpr uint32_t Q_DC = 128 * 128;                // one 64-column chunk of Q (128 rows)
-    static constexpr uint32_t Q_BYTES = (D / 64) * Q_DC;       // Q tile
-    static constexpr uint32_t P_BYTES = 128 * KT * 2;          // P of one chunk, 128 rows
+    static constexpr uint32_t HALF_DC = 128 * 128;             // 128 rows x 64 columns of Q
+    static constexpr uint32_t Q_DC = 2 * HALF_DC;              // both halves, one column chunk
+    static constexpr uint32_t Q_BYTES = (D / 64) * Q_DC;
+    static constexpr uint32_t P_BYTES = 128 * KT * 2;          // P of one chunk, one half
     static constexpr uint32_t KV_DC = KT * 128;                // 64 keys x 64 columns
     static constexpr uint32_t STG = (D / 64) * KV_DC;          // K or V of one chunk
-    static constexpr uint32_t OFF_P = Q_BYTES;
-    static constexpr uint32_t OFF_STAGES = OFF_P + 2 * P_BYTES;
-    static constexpr uint32_t TMEM_COLS = 256;                 // S[2] (2 x 64) + O (<= 128)
+    static constexpr uint32_t OFF_P = Q_BYTES;                 // [half][buffer]
+    static constexpr uint32_t OFF_STAGES = OFF_P + 4 * P_BYTES;
+    static constexpr uint32_t TMEM_COLS = 512;                 // per half: S[2] (2 x 64) + O
+    static constexpr uint32_t HALF_COLS = 256;
     static constexpr uint32_t COL_O = 128;
 };
 
@@ -225,6 +229,7 @@ struct Segment {
     int64_t end;     // one past the segment's last unit
     int nblk;        // blocks in the segment
     int chunks;      // ceil(nblk / 4)
+    int tile_tokens; // query tokens of the tile
 };
 
 __device__ __forceinline__ void segment_at(const PrefillArgs &a, const int64_t *pre, int64_t f,
@@ -233,10 +238,11 @@ __device__ __forceinline__ void segment_at(const PrefillArgs &a, const int64_t *
     sg.end = min64(hi, sg.u.tile_begin + sg.u.tile_blocks);
     sg.nblk = (int)(sg.end - f);
     sg.chunks = (sg.nblk + 3) / 4;
+    sg.tile_tokens = (int)min64(a.tokens_per_tile, sg.u.t.q_len - sg.u.qt * a.tokens_per_tile);
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
@@ -251,28 +257,30 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     const int NST = a.num_stages;
     uint8_t *sQ = smem, *sP = smem + L::OFF_P, *sStage = smem + L::OFF_STAGES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)NST * L::STG);
-    uint64_t *q_full = bars, *q_empty = bars + 1, *s_full = bars + 2, *p_full = bars + 4,
-             *pv_done = bars + 6, *o_free = bars + 8, *mma_done = bars + 9;
-    uint64_t *kv_full = bars + 10, *kv_empty = kv_full + NST;
+    // per half h: s_full[h][2], p_full[h][2], pv_done[h][2], o_free[h]
+    uint64_t *q_full = bars, *q_empty = bars + 1, *mma_done = bars + 2;
+    uint64_t *s_full = bars + 3, *p_full = bars + 7, *pv_done = bars + 11, *o_free = bars + 15;
+    uint64_t *kv_full = bars + 17, *kv_empty = kv_full + NST;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(kv_empty + NST);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int64_t *scan_tmp = reinterpret_cast<int64_t *>(tmem_slot + 2);  // 32 entries
     int64_t *pre = scan_tmp + 32;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int group = a.group, TPT = a.tokens_per_tile;
-    const int tile_rows = TPT * group;
+    const int group = a.group, TPT = a.tokens_per_tile, HTOK = TPT / 2;
+    const int tile_rows = TPT * group, half_rows = HTOK * group;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        mbar_init(mma_done, 1);
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
             mbar_init(&pv_done[i], 1);
         }
-        mbar_init(o_free, 128);
-        mbar_init(mma_done, 1);
+        mbar_init(&o_free[0], 128);
+        mbar_init(&o_free[1], 128);
         for (int i = 0; i < NST; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -304,7 +312,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         const uint64_t policy = l2_policy_evict_normal();
-        uint32_t fill = 0;
+        uint32_t fill = 0, pst = 0, pph = 0;  // copies issued; ring slot of the next one
         int seg_i = 0;
         bool ok = true;
         for (int64_t f = lo; f < hi && ok;) {
@@ -314,10 +322,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             if (lane == 0) {
                 if (seg_i > 0) ok = mbar_wait(q_empty, (seg_i - 1) & 1, abort_flag);
                 if (ok) {
-                    mbar_arrive_expect_tx(q_full, DCH * tile_rows * 128);
-                    for (int dc = 0; dc < DCH; ++dc)
-                        tma_load_4d(sQ + dc * L::Q_DC, &q_map, q_full, 0, dc, u.kvh * group,
-                                    (int)(u.t.q_row0 + u.qt * TPT), policy);
+                    mbar_arrive_expect_tx(q_full, 2 * DCH * half_rows * 128);
+                    const int tok0 = (int)(u.t.q_row0 + u.qt * TPT);
+                    for (int h = 0; h < 2; ++h)
+                        for (int dc = 0; dc < DCH; ++dc)
+                            tma_load_4d(sQ + dc * L::Q_DC + h * L::HALF_DC, &q_map, q_full, 0, dc,
+                                        u.kvh * group, tok0 + h * HTOK, policy);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -342,11 +352,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (lane == 0) {
 #pragma unroll
                         for (int kv = 0; kv < 2; ++kv) {
-                            const uint32_t st = fill % NST, round = fill / NST;
-                            if (!mbar_wait(&kv_empty[st], (round & 1) ^ 1, abort_flag)) {
+                            const uint32_t st = pst;
+                            if (!mbar_wait(&kv_empty[st], pph ^ 1, abort_flag)) {
                                 ok = false;
                                 break;
                             }
+                            if (++pst == (uint32_t)NST) { pst = 0; pph ^= 1; }
                             mbar_arrive_expect_tx(&kv_full[st], L::STG);
                             uint8_t *dst = sStage + (size_t)st * L::STG;
                             const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
@@ -377,57 +388,94 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t tS = tmem, tO = tmem + L::COL_O;
-            uint32_t g = 0;
+            // The issue loop is on the critical path, so nothing in it divides or builds a
+            // descriptor from scratch: descriptors are base values advanced by constant
+            // 16-byte-unit offsets, and the K/V ring position is a (stage, phase) pair.
+            const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = umma_desc_sw128(smem_u32(sStage), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(sStage), L::KV_DC, 1024);
+            const uint64_t dp0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
+            constexpr uint32_t STG16 = L::STG >> 4;
+            uint32_t kst = 0, kph = 0;  // ring slot of the next K chunk
+            uint32_t gh[2] = {0, 0};    // chunks each half has processed
+            int segh[2] = {0, 0};       // segments each half has processed
             int seg_i = 0;
             bool ok = true;
-            auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-                if (first && seg_i > 0 && !mbar_wait(o_free, (seg_i - 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(&p_full[gp & 1], (gp >> 1) & 1, abort_flag)) return false;
-                const uint32_t vf = 2 * gp + 1;
-                if (!mbar_wait(&kv_full[vf % NST], (vf / NST) & 1, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t pa = smem_u32(sP + (gp & 1) * L::P_BYTES);
-                const uint32_t va = smem_u32(sStage + (size_t)(vf % NST) * L::STG);
-#pragma unroll
-                for (int ks = 0; ks < L::KT / 16; ++ks)
-                    umma_bf16(tO, umma_desc_sw128(pa + ks * 32, 16, 1024),
-                              umma_desc_sw128(va + ks * 2048, L::KV_DC, 1024), IDESC_PV,
-                              !(first && ks == 0));
-                umma_commit(&pv_done[gp & 1]);
-                umma_commit(&kv_empty[vf % NST]);
-                return true;
+            bool issued = false;
+            auto adv = [&](uint32_t &st, uint32_t &ph) {
+                if (++st == (uint32_t)NST) { st = 0; ph ^= 1; }
             };
             for (int64_t f = lo; f < hi && ok;) {
                 Segment sg;
                 segment_at(a, pre, f, hi, sg);
+                const int nh = sg.tile_tokens > HTOK ? 2 : 1;  // halves with query rows
                 ok = mbar_wait(q_full, seg_i & 1, abort_flag);
                 tc_fence_after();
-                const uint32_t qa = smem_u32(sQ);
-                for (int ch = 0; ch < sg.chunks && ok; ++ch, ++g) {
-                    if (g >= 2 && !mbar_wait(&p_full[g & 1], ((g - 2) >> 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t kf = 2 * g;
-                    if (!mbar_wait(&kv_full[kf % NST], (kf / NST) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t ka = smem_u32(sStage + (size_t)(kf % NST) * L::STG);
+                // O += P V for the segment's chunk chp (V in ring slot vst), every half.
+                auto issue_pv = [&](int chp, uint32_t vst, uint32_t vph) -> bool {
+                    if (!mbar_wait(&kv_full[vst], vph, abort_flag)) return false;
+                    const uint64_t dv = dv0 + vst * STG16;
+                    for (int h = 0; h < nh; ++h) {
+                        const uint32_t gg = gh[h] + chp;
+                        const int pb = 2 * h + (gg & 1);
+                        if (chp == 0 && segh[h] > 0 && !mbar_wait(&o_free[h], (segh[h] - 1) & 1, abort_flag))
+                            return false;
+                        if (!mbar_wait(&p_full[pb], (gg >> 1) & 1, abort_flag)) return false;
+                        tc_fence_after();
+                        const uint64_t dp = dp0 + pb * (L::P_BYTES >> 4);
+                        const uint32_t tO = tmem + h * L::HALF_COLS + L::COL_O;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t dc = ks / 4, ko = (ks % 4) * 32;
-                        umma_bf16(tS + (g & 1) * L::KT, umma_desc_sw128(qa + dc * L::Q_DC + ko, 16, 1024),
-                                  umma_desc_sw128(ka + dc * L::KV_DC + ko, 16, 1024), IDESC_QK, ks > 0);
+                        for (int ks = 0; ks < L::KT / 16; ++ks)
+                            umma_bf16(tO, dp + ks * 2, dv + ks * (2048 >> 4), IDESC_PV, !(chp == 0 && ks == 0));
+                        umma_commit(&pv_done[pb]);
                     }
-                    umma_commit(&s_full[g & 1]);
-                    umma_commit(&kv_empty[kf % NST]);
+                    umma_commit(&kv_empty[vst]);
+                    return true;
+                };
+                uint32_t pvst = 0, pvph = 0;  // ring slot of the previous chunk's V
+                for (int ch = 0; ch < sg.chunks && ok; ++ch) {
+                    const uint32_t cst = kst, cph = kph;  // this chunk's K
+                    uint32_t vst = kst, vph = kph;        // and V (the next ring slot)
+                    adv(vst, vph);
+                    kst = vst;
+                    kph = vph;
+                    adv(kst, kph);                        // the next chunk's K
+                    if (!mbar_wait(&kv_full[cst], cph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t dk = dk0 + cst * STG16;
+                    for (int h = 0; h < nh && ok; ++h) {
+                        const uint32_t gg = gh[h] + ch;
+                        const int sb = 2 * h + (gg & 1);
+                        if (gg >= 2 && !mbar_wait(&p_full[sb], ((gg - 2) >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dq = dq0 + h * (L::HALF_DC >> 4);
+                        const uint32_t tS = tmem + h * L::HALF_COLS + (gg & 1) * L::KT;
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t off = ((ks / 4) * L::KV_DC + (ks % 4) * 32) >> 4;
+                            const uint32_t qoff = ((ks / 4) * L::Q_DC + (ks % 4) * 32) >> 4;
+                            umma_bf16(tS, dq + qoff, dk + off, IDESC_QK, ks > 0);
+                        }
+                        umma_commit(&s_full[sb]);
+                        issued = true;
+                    }
+                    if (!ok) break;
+                    umma_commit(&kv_empty[cst]);
                     if (ch == sg.chunks - 1) umma_commit(q_empty);
-                    if (ch >= 1 && !issue_pv(g - 1, ch == 1)) ok = false;
+                    if (ch >= 1 && !issue_pv(ch - 1, pvst, pvph)) ok = false;
+                    pvst = vst;
+                    pvph = vph;
                 }
-                if (ok && !issue_pv(g - 1, sg.chunks == 1)) ok = false;
+                if (ok && !issue_pv(sg.chunks - 1, pvst, pvph)) ok = false;
+                for (int h = 0; h < nh; ++h) {
+                    gh[h] += sg.chunks;
+                    segh[h] += 1;
+                }
                 f = sg.end;
                 ++seg_i;
             }
@@ -436,59 +484,76 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 *abort_flag = 1;
             }
             // every MMA this thread issued is finished before TMEM is released
-            umma_commit(mma_done);
-            mbar_wait(mma_done, 0, nullptr);
+            if (issued) {
+                umma_commit(mma_done);
+                mbar_wait(mma_done, 0, nullptr);
+            }
         }
         __syncwarp();
     } else {
-        // ----------------------- softmax (one thread per row) -----------------------
+        // -------------- softmax: one warpgroup per half, one row per thread --------------
+        const int h = (warp - 2) >> 2;
         const int quarter = warp & 3;  // the TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + tl, tO = tmem + tl + L::COL_O;
-        const int tid = threadIdx.x - 64;  // 0..127
+        const uint32_t tS = tmem + tl + h * L::HALF_COLS;
+        const uint32_t tO = tmem + tl + h * L::HALF_COLS + L::COL_O;
+        const int tid = threadIdx.x - 64 - 128 * h;  // 0..127 within the warpgroup
         const float sl2 = a.scale_log2;
-        uint32_t g = 0;
-        int seg_i = 0;
+        uint32_t gh = 0;   // chunks this half has processed
+        uint32_t gk = 0;   // chunks of the CTA (K/V ring position)
+        int segh = 0;
         bool ok = true;
         for (int64_t f = lo; f < hi && ok;) {
             Segment sg;
             segment_at(a, pre, f, hi, sg);
             const UnitPos &u = sg.u;
+            if (h == 1 && sg.tile_tokens <= HTOK) {  // this half has no query rows here
+                gk += sg.chunks;
+                f = sg.end;
+                continue;
+            }
             const int ctx = u.t.ctx;
-            const int tile_tokens = (int)min64(TPT, u.t.q_len - u.qt * TPT);
-            const int tok = row / group, hg = row - tok * group;
-            const bool rvalid = row < tile_rows && tok < tile_tokens;
+            const int half_tokens = min(HTOK, sg.tile_tokens - h * HTOK);
+            const int tok_l = row / group, hg = row - tok_l * group;
+            const bool rvalid = row < half_rows && tok_l < half_tokens;
+            const int tok = h * HTOK + tok_l;  // token inside the tile
             const int64_t first_pos = (int64_t)(ctx - u.t.q_len) + u.qt * TPT;
-            const int64_t lim = a.causal ? min64(first_pos + min(tok, tile_tokens - 1) + 1, ctx) : ctx;
+            const int64_t lim =
+                a.causal ? min64(first_pos + min(tok, sg.tile_tokens - 1) + 1, ctx) : ctx;
             float m_ref = -INFINITY, l = 0.f;
-            for (int ch = 0; ch < sg.chunks; ++ch, ++g) {
+            for (int ch = 0; ch < sg.chunks; ++ch, ++gh, ++gk) {
                 const int nb = min(L::BPC, sg.nblk - L::BPC * ch);
                 const int64_t key0 = (u.kb + (int64_t)L::BPC * ch) * kBS;
                 const int nkeys = nb * kBS;
-                if (!mbar_wait(&s_full[g & 1], (g >> 1) & 1, abort_flag)) { ok = false; break; }
+                const int bsel = 2 * h + (gh & 1);
+                if (!mbar_wait(&s_full[bsel], (gh >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[2][32];
-                tmem_ld32(tS + (g & 1) * L::KT, sr[0]);
-                tmem_ld32(tS + (g & 1) * L::KT + 32, sr[1]);
+                tmem_ld32(tS + (gh & 1) * L::KT, sr[0]);
+                tmem_ld32(tS + (gh & 1) * L::KT + 32, sr[1]);
                 tmem_wait_ld();
-                // visible keys of this chunk for this row: [0, vis)
                 const int vis = (int)max64(0, min64(lim - key0, (int64_t)nkeys));
-                float sv[64];
-                float mx = -INFINITY;
+                float v[64];
+                if (__all_sync(0xffffffffu, vis >= 64)) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float x = __uint_as_float(sr[j >> 5][j & 31]) * sl2;
-                    sv[j] = j < vis ? x : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(sr[j >> 5][j & 31]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) v[j] = j < vis ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
                 }
+                float m4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+                for (int j = 4; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
+                // raw maximum, then scaled (scale > 0 keeps the order; -inf stays -inf)
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
                 const bool up = mx > m_ref + kRescaleSlack;
                 if (__any_sync(0xffffffffu, up)) {
                     const float alpha = up ? fast_exp2(m_ref - mx) : 1.f;
                     if (ch > 0) {
                         // O holds this segment's earlier chunks: wait for the last PV, rescale.
-                        const uint32_t gp = g - 1;
-                        if (!mbar_wait(&pv_done[gp & 1], (gp >> 1) & 1, abort_flag)) { ok = false; break; }
+                        const uint32_t gp = gh - 1;
+                        if (!mbar_wait(&pv_done[2 * h + (gp & 1)], (gp >> 1) & 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int q = 0; q < D / 32; ++q) {
@@ -505,25 +570,29 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (up) m_ref = mx;
                 }
                 const float base = m_ref == -INFINITY ? 0.f : m_ref;
-                uint32_t pk[32];
-                float ps = 0.f;
+                // P buffer bsel is free once PV(gh - 2) has read it
+                if (gh >= 2 && !mbar_wait(&pv_done[bsel], ((gh - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+                uint8_t *prow = sP + bsel * L::P_BYTES + row * 128;
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    pk[j] = pack_bf16x2(fast_exp2(sv[2 * j] - base), fast_exp2(sv[2 * j + 1] - base));
-                    ps += bf16_lo(pk[j]) + bf16_hi(pk[j]);
-                }
-                l += ps;
-                // P buffer g & 1 is free once PV(g - 2) has read it
-                if (g >= 2 && !mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-                uint8_t *prow = sP + (g & 1) * L::P_BYTES + row * 128;
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    uint32_t pk[4];
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16)
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 8 * c16 + 2 * e;
+                        pk[e] = pack_bf16x2(fast_exp2(fmaf(v[j], sl2, -base)),
+                                            fast_exp2(fmaf(v[j + 1], sl2, -base)));
+                        ps[e] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                    }
                     *reinterpret_cast<uint4 *>(prow + ((c16 ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-                if (key0 + nkeys > ctx) {
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                if (h == 0 && key0 + nkeys > ctx) {
                     // The chunk runs past the context: the pool rows there may hold NaN, and
-                    // 0 * NaN would poison O, so zero those V rows before PV reads them.
-                    const uint32_t vf = 2 * g + 1;
+                    // 0 * NaN would poison O, so zero those V rows before PV reads them (the
+                    // second half's PV is issued after the first half's, so it sees them too).
+                    const uint32_t vf = 2 * gk + 1;
                     if (!mbar_wait(&kv_full[vf % NST], (vf / NST) & 1, abort_flag)) { ok = false; break; }
                     uint8_t *vst = sStage + (size_t)(vf % NST) * L::STG;
                     const int r0 = (int)(ctx - key0), nrows = nkeys - r0;
@@ -535,19 +604,20 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(&p_full[g & 1]);
+                mbar_arrive(&p_full[bsel]);
             }
             if (!ok) break;
             // ---- epilogue: O / l for the tile, or the part for the merge ----
-            const uint32_t gl = g - 1;
-            if (!mbar_wait(&pv_done[gl & 1], (gl >> 1) & 1, abort_flag)) { ok = false; break; }
+            const uint32_t gl = gh - 1;
+            if (!mbar_wait(&pv_done[2 * h + (gl & 1)], (gl >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const bool whole = lo <= u.tile_begin && sg.end == u.tile_begin + u.tile_blocks;
             const float inv = 1.f / l;
             const int64_t qrow = u.t.q_row0 + u.qt * TPT + tok;
             __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)u.kvh * group + hg) * D;
             const int slot = whole ? 0 : part_slot(c, u.tile_begin, T, ge);
-            float *wrow = a.ws_o + ((int64_t)slot * tile_rows + row) * D;
+            const int trow = tok * group + hg;  // row inside the tile
+            float *wrow = a.ws_o + ((int64_t)slot * tile_rows + trow) * D;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t r[32];
@@ -557,12 +627,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (whole) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + q * 32 + j) = v;
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+                        o.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+                        o.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
+                        o.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + q * 32 + j) = o;
                     }
                 } else {
 #pragma unroll
@@ -570,11 +640,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                         *reinterpret_cast<uint4 *>(wrow + q * 32 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
                 }
             }
-            if (!whole && rvalid) a.ws_ml[(int64_t)slot * tile_rows + row] = make_float2(m_ref, l);
+            if (!whole && rvalid) a.ws_ml[(int64_t)slot * tile_rows + trow] = make_float2(m_ref, l);
             tc_fence_before();
-            mbar_arrive(o_free);
+            mbar_arrive(&o_free[h]);
             f = sg.end;
-            ++seg_i;
+            ++segh;
         }
         if (!ok) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -595,14 +665,15 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     if (num_kv_heads <= 0 || num_heads % num_kv_heads) return PKV_ERR_UNSUPPORTED;
     p->group = num_heads / num_kv_heads;
     if (p->group > 8) return PKV_ERR_UNSUPPORTED;
-    p->tokens_per_tile = 16 * (8 / p->group);  // 128 / group rounded down to 16 tokens
-    p->rows = p->tokens_per_tile * p->group;    // <= 128 = the MMA's M
-    p->warps = 6;
+    // A tile is two halves of 16 * (8 / group) tokens x group heads (<= 128 rows each).
+    p->tokens_per_tile = 2 * 16 * (8 / p->group);
+    p->rows = p->tokens_per_tile * p->group;    // <= 256 rows per tile
+    p->warps = 10;  // producer, MMA issuer, one softmax warpgroup per half
     p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
-    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 128 * 128, p_bytes = 2 * 128 * 64 * 2;
+    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128, p_bytes = 4 * 128 * 64 * 2;
     p->stage_bytes = 64 * head_dim * 2;
-    const size_t fixed = 1024 + q_bytes + p_bytes + 8 * 10 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
+    const size_t fixed = 1024 + q_bytes + p_bytes + 8 * 17 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
     int nst = (int)(((int64_t)smem_optin - (int64_t)fixed) / (p->stage_bytes + 16));
     if (nst > 8) nst = 8;
     if (nst < 4) return PKV_ERR_UNSUPPORTED;
