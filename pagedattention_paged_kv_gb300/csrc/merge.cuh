@@ -37,7 +37,7 @@ struct MergeArgs {
     int num_heads;
 };
 
-constexpr int kMergeMaxRows = 32;    // rows per CTA; a job gets ceil(slot_rows / 32) CTAs
+constexpr int kMergeMaxRows = 16;    // rows per CTA; a job gets ceil(slot_rows / 16) CTAs
 constexpr int kMergeSmemParts = 32;  // parts whose (m, l) and weight stay in shared memory
 
 __device__ __forceinline__ void no_job(MergeJob &j) {
