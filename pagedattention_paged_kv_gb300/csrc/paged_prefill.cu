@@ -10,17 +10,22 @@
 // "vLLM推理引擎架构PagedAttention机制与高吞吐推理" (lpnh.cn), §2.3.
 //
 // GB300 design
-//  * A tile is 16 query tokens x the `group` query heads of one KV head (128 rows for
-//    Llama-70B shapes): one K/V block read from shared memory feeds 128 query rows,
-//    enough reuse for the work to be tensor-bound.  Eight consumer warps each own 16
-//    rows and run S = Q K^T and O += P V as m16n8k16 bf16 MMAs with fp32 accumulation
-//    and an fp32 online softmax; the S fragments become the P operand directly.
+//  * A tile is 2 halves x (16 * 8 / group) query tokens x the `group` query heads of one
+//    KV head, i.e. two 128-row tcgen05 MMA tiles for Llama-70B shapes; both halves use
+//    every K/V chunk in shared memory, so a key is read from L2 once per 256 query rows.
+//  * Keys go in 128-key chunks (8 blocks).  One elected thread issues S = Q K^T
+//    (128 x 128 x head_dim, A and B from 128-byte-swizzled shared memory) into TMEM, the
+//    half's softmax warpgroup (one thread per row) reads the row's 128 scores in one
+//    TMEM round trip, writes the bf16 weights P back over S, and O += P V runs with P as
+//    the A operand straight from TMEM.  The halves alternate on the tensor pipe, so one
+//    half's MMAs overlap the other half's softmax.  Online softmax in base 2, rescaled
+//    only when a row's maximum grows by more than 2^8 (O is then rescaled in TMEM).
 //  * The units are (tile, 16-token key block) pairs; causal tiles stop at the block
 //    holding their last query's position.  A persistent grid (one CTA per SM) takes
 //    equal contiguous shares of the flat unit list, so long prefixes split across
 //    CTAs and no SM idles in a tail; split tiles are merged by log-sum-exp weights.
-//  * A producer warp streams each key block (K, then V, of one KV head: 16 rows x
-//    head_dim) with TMA into a ring of 128-byte-swizzled shared-memory stages.
+//  * A producer warp streams K and V of each chunk with TMA (one 5-D box per block and
+//    64-column slice) into a ring of shared-memory stages.
 //  * Waits are bounded in time; no CTA waits on another CTA.
 #include "attn_block.cuh"
 #include "merge.cuh"
@@ -33,6 +38,19 @@ namespace pkv {
 namespace {
 
 constexpr int kBS = 16;
+
+// 12 warps: warpgroup 0 = TMA producer, tcgen05 issuer and two idle warps; warpgroups 1
+// and 2 = softmax of the tile's two halves.  Launched at 168 registers a thread (the most
+// 12 warps may hold); a split (warpgroup 0 down to kPrefillRegsLow, the softmax up to
+// kPrefillRegsHigh) is applied only when the two differ.  Measured on the 512-token chunk:
+// 112/192 and 80/208 run 2-3x slower (the issuer and producer spill), so both stay at 168.
+// The host checks before every launch that the launch pool covers the split (a rise the
+// pool cannot cover would wait forever).
+constexpr int kPrefillThreads = 384;
+constexpr int kPrefillRegsLow = 168;
+constexpr int kPrefillRegsHigh = 168;
+static_assert(128 * kPrefillRegsLow + 256 * kPrefillRegsHigh <= kPrefillThreads * 168,
+              "register split exceeds the launch pool");
 
 // Closed forms for one sequence's tiles.  Tile qt covers query tokens
 // [qt*TPT, min(q_len, (qt+1)*TPT)).  Causal: the tile visits key blocks
@@ -207,42 +225,42 @@ __device__ void write_jobs_and_invalid_rows(const PrefillArgs &a, const int64_t 
 // every K/V chunk the producer loads.
 template <int D>
 struct PrefillSmem {
-    static constexpr int KT = 64;                              // keys per chunk
+    static constexpr int KT = 128;                             // keys per chunk (the QK MMA's N)
     static constexpr int BPC = KT / kBS;                       // blocks per chunk
     static constexpr uint32_t HALF_DC = 128 * 128;             // 128 rows x 64 columns of Q
     static constexpr uint32_t Q_DC = 2 * HALF_DC;              // both halves, one column chunk
     static constexpr uint32_t Q_BYTES = (D / 64) * Q_DC;
-    static constexpr uint32_t P_BYTES = 128 * KT * 2;          // P of one chunk, one half
-    static constexpr uint32_t KV_DC = KT * 128;                // 64 keys x 64 columns
+    static constexpr uint32_t KV_DC = KT * 128;                // 128 keys x 64 columns
     static constexpr uint32_t STG = (D / 64) * KV_DC;          // K or V of one chunk
-    static constexpr uint32_t OFF_P = Q_BYTES;                 // [half][buffer]
-    static constexpr uint32_t OFF_STAGES = OFF_P + 4 * P_BYTES;
-    static constexpr uint32_t TMEM_COLS = 512;                 // per half: S[2] (2 x 64) + O
+    static constexpr uint32_t OFF_STAGES = Q_BYTES;
+    // TMEM, per half: S (128 fp32 columns; P overwrites its first 64 as bf16 pairs), O.
+    static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t HALF_COLS = 256;
     static constexpr uint32_t COL_O = 128;
 };
 
 // The CTA's share is walked segment by segment (a segment = the part of one tile that
-// lies in the share); each segment's blocks go in chunks of up to 4 (64 keys).
+// lies in the share); each segment's blocks go in chunks of up to BPC.
 struct Segment {
     UnitPos u;
     int64_t end;     // one past the segment's last unit
     int nblk;        // blocks in the segment
-    int chunks;      // ceil(nblk / 4)
+    int chunks;      // ceil(nblk / BPC)
     int tile_tokens; // query tokens of the tile
 };
 
+template <int BPC>
 __device__ __forceinline__ void segment_at(const PrefillArgs &a, const int64_t *pre, int64_t f,
                                            int64_t hi, Segment &sg) {
     locate(a, pre, f, sg.u);
     sg.end = min64(hi, sg.u.tile_begin + sg.u.tile_blocks);
     sg.nblk = (int)(sg.end - f);
-    sg.chunks = (sg.nblk + 3) / 4;
+    sg.chunks = (sg.nblk + BPC - 1) / BPC;
     sg.tile_tokens = (int)min64(a.tokens_per_tile, sg.u.t.q_len - sg.u.qt * a.tokens_per_tile);
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kPrefillThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
@@ -255,12 +273,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = a.num_stages;
-    uint8_t *sQ = smem, *sP = smem + L::OFF_P, *sStage = smem + L::OFF_STAGES;
+    uint8_t *sQ = smem, *sStage = smem + L::OFF_STAGES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)NST * L::STG);
-    // per half h: s_full[h][2], p_full[h][2], pv_done[h][2], o_free[h]
+    // per half h: s_full[h], p_full[h], pv_done[h], o_free[h]
     uint64_t *q_full = bars, *q_empty = bars + 1, *mma_done = bars + 2;
-    uint64_t *s_full = bars + 3, *p_full = bars + 7, *pv_done = bars + 11, *o_free = bars + 15;
-    uint64_t *kv_full = bars + 17, *kv_empty = kv_full + NST;
+    uint64_t *s_full = bars + 3, *p_full = bars + 5, *pv_done = bars + 7, *o_free = bars + 9;
+    uint64_t *kv_full = bars + 11, *kv_empty = kv_full + NST;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(kv_empty + NST);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int64_t *scan_tmp = reinterpret_cast<int64_t *>(tmem_slot + 2);  // 32 entries
@@ -274,13 +292,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         mbar_init(mma_done, 1);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
-            mbar_init(&pv_done[i], 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 128);
+            mbar_init(&pv_done[h], 1);
+            mbar_init(&o_free[h], 128);
         }
-        mbar_init(&o_free[0], 128);
-        mbar_init(&o_free[1], 128);
         for (int i = 0; i < NST; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -309,6 +326,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Warpgroup 0 (producer, MMA issuer, two idle warps) gives registers to the two
+    // softmax warpgroups, which hold a row's 128 scores in registers.
+    if constexpr (kPrefillRegsLow != kPrefillRegsHigh) {
+        if (warp < 4) reg_dealloc<kPrefillRegsLow>();
+        else reg_alloc<kPrefillRegsHigh>();
+    }
+
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         const uint64_t policy = l2_policy_evict_normal();
@@ -317,7 +341,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         bool ok = true;
         for (int64_t f = lo; f < hi && ok;) {
             Segment sg;
-            segment_at(a, pre, f, hi, sg);
+            segment_at<L::BPC>(a, pre, f, hi, sg);
             const UnitPos &u = sg.u;
             if (lane == 0) {
                 if (seg_i > 0) ok = mbar_wait(q_empty, (seg_i - 1) & 1, abort_flag);
@@ -387,16 +411,18 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
+        // Per half h, S lives in TMEM columns [h*256, h*256+128); the softmax writes the bf16
+        // weights P back over its first 64 columns, and PV takes them as the A operand from
+        // TMEM.  The halves alternate on the tensor pipe: PV_0(c), QK_0(c+1), PV_1(c),
+        // QK_1(c+1), so one half's MMAs run while the other half's softmax works.  QK_h(c+1)
+        // overwrites S_h right after PV_h(c) read P_h from it; MMAs of one thread run in issue
+        // order, and the softmax learns both are done from the commit behind QK_h(c+1).
         if (lane == 0) {
-            // The issue loop is on the critical path, so nothing in it divides or builds a
-            // descriptor from scratch: descriptors are base values advanced by constant
-            // 16-byte-unit offsets, and the K/V ring position is a (stage, phase) pair.
             const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(smem_u32(sStage), 16, 1024);
             const uint64_t dv0 = umma_desc_sw128(smem_u32(sStage), L::KV_DC, 1024);
-            const uint64_t dp0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
             constexpr uint32_t STG16 = L::STG >> 4;
-            uint32_t kst = 0, kph = 0;  // ring slot of the next K chunk
+            uint32_t kst = 0, kph = 0;  // ring slot of the next chunk's K
             uint32_t gh[2] = {0, 0};    // chunks each half has processed
             int segh[2] = {0, 0};       // segments each half has processed
             int seg_i = 0;
@@ -405,73 +431,75 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             auto adv = [&](uint32_t &st, uint32_t &ph) {
                 if (++st == (uint32_t)NST) { st = 0; ph ^= 1; }
             };
+            auto issue_qk = [&](int h, uint32_t kslot) {
+                const uint64_t dk = dk0 + kslot * STG16;
+                const uint64_t dq = dq0 + h * (L::HALF_DC >> 4);
+                const uint32_t tS = tmem + h * L::HALF_COLS;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = ((ks / 4) * L::KV_DC + (ks % 4) * 32) >> 4;
+                    const uint32_t qoff = ((ks / 4) * L::Q_DC + (ks % 4) * 32) >> 4;
+                    umma_bf16(tS, dq + qoff, dk + koff, IDESC_QK, ks > 0);
+                }
+                umma_commit(&s_full[h]);
+                issued = true;
+            };
             for (int64_t f = lo; f < hi && ok;) {
                 Segment sg;
-                segment_at(a, pre, f, hi, sg);
+                segment_at<L::BPC>(a, pre, f, hi, sg);
                 const int nh = sg.tile_tokens > HTOK ? 2 : 1;  // halves with query rows
-                ok = mbar_wait(q_full, seg_i & 1, abort_flag);
+                if (!mbar_wait(q_full, seg_i & 1, abort_flag)) { ok = false; break; }
+                // chunk 0's K and V slots
+                uint32_t ks_ = kst, kp_ = kph;
+                uint32_t vs_ = kst, vp_ = kph;
+                adv(vs_, vp_);
+                kst = vs_;
+                kph = vp_;
+                adv(kst, kph);
+                if (!mbar_wait(&kv_full[ks_], kp_, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                // O += P V for the segment's chunk chp (V in ring slot vst), every half.
-                auto issue_pv = [&](int chp, uint32_t vst, uint32_t vph) -> bool {
-                    if (!mbar_wait(&kv_full[vst], vph, abort_flag)) return false;
-                    const uint64_t dv = dv0 + vst * STG16;
-                    for (int h = 0; h < nh; ++h) {
-                        const uint32_t gg = gh[h] + chp;
-                        const int pb = 2 * h + (gg & 1);
-                        if (chp == 0 && segh[h] > 0 && !mbar_wait(&o_free[h], (segh[h] - 1) & 1, abort_flag))
-                            return false;
-                        if (!mbar_wait(&p_full[pb], (gg >> 1) & 1, abort_flag)) return false;
-                        tc_fence_after();
-                        const uint64_t dp = dp0 + pb * (L::P_BYTES >> 4);
-                        const uint32_t tO = tmem + h * L::HALF_COLS + L::COL_O;
-#pragma unroll
-                        for (int ks = 0; ks < L::KT / 16; ++ks)
-                            umma_bf16(tO, dp + ks * 2, dv + ks * (2048 >> 4), IDESC_PV, !(chp == 0 && ks == 0));
-                        umma_commit(&pv_done[pb]);
-                    }
-                    umma_commit(&kv_empty[vst]);
-                    return true;
-                };
-                uint32_t pvst = 0, pvph = 0;  // ring slot of the previous chunk's V
+                for (int h = 0; h < nh; ++h) issue_qk(h, ks_);
+                umma_commit(&kv_empty[ks_]);
+                if (sg.chunks == 1) umma_commit(q_empty);
                 for (int ch = 0; ch < sg.chunks && ok; ++ch) {
-                    const uint32_t cst = kst, cph = kph;  // this chunk's K
-                    uint32_t vst = kst, vph = kph;        // and V (the next ring slot)
-                    adv(vst, vph);
-                    kst = vst;
-                    kph = vph;
-                    adv(kst, kph);                        // the next chunk's K
-                    if (!mbar_wait(&kv_full[cst], cph, abort_flag)) {
-                        ok = false;
-                        break;
+                    const bool more = ch + 1 < sg.chunks;
+                    uint32_t nks = kst, nkp = kph;  // the next chunk's K and V slots
+                    uint32_t nvs = kst, nvp = kph;
+                    if (more) {
+                        adv(nvs, nvp);
+                        kst = nvs;
+                        kph = nvp;
+                        adv(kst, kph);
                     }
-                    const uint64_t dk = dk0 + cst * STG16;
+                    if (!mbar_wait(&kv_full[vs_], vp_, abort_flag)) { ok = false; break; }
+                    if (more && !mbar_wait(&kv_full[nks], nkp, abort_flag)) { ok = false; break; }
+                    const uint64_t dv = dv0 + vs_ * STG16;
                     for (int h = 0; h < nh && ok; ++h) {
                         const uint32_t gg = gh[h] + ch;
-                        const int sb = 2 * h + (gg & 1);
-                        if (gg >= 2 && !mbar_wait(&p_full[sb], ((gg - 2) >> 1) & 1, abort_flag)) {
+                        if (ch == 0 && segh[h] > 0 && !mbar_wait(&o_free[h], (segh[h] - 1) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
+                        if (!mbar_wait(&p_full[h], gg & 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        const uint64_t dq = dq0 + h * (L::HALF_DC >> 4);
-                        const uint32_t tS = tmem + h * L::HALF_COLS + (gg & 1) * L::KT;
+                        const uint32_t tP = tmem + h * L::HALF_COLS;
+                        const uint32_t tO = tP + L::COL_O;
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t off = ((ks / 4) * L::KV_DC + (ks % 4) * 32) >> 4;
-                            const uint32_t qoff = ((ks / 4) * L::Q_DC + (ks % 4) * 32) >> 4;
-                            umma_bf16(tS, dq + qoff, dk + off, IDESC_QK, ks > 0);
-                        }
-                        umma_commit(&s_full[sb]);
-                        issued = true;
+                        for (int ks = 0; ks < L::KT / 16; ++ks)
+                            umma_bf16_tmem_a(tO, tP + ks * 8, dv + ks * (2048 >> 4), IDESC_PV,
+                                             !(ch == 0 && ks == 0));
+                        umma_commit(&pv_done[h]);
+                        if (more) issue_qk(h, nks);
                     }
                     if (!ok) break;
-                    umma_commit(&kv_empty[cst]);
-                    if (ch == sg.chunks - 1) umma_commit(q_empty);
-                    if (ch >= 1 && !issue_pv(ch - 1, pvst, pvph)) ok = false;
-                    pvst = vst;
-                    pvph = vph;
+                    umma_commit(&kv_empty[vs_]);
+                    if (more) {
+                        umma_commit(&kv_empty[nks]);
+                        if (ch + 1 == sg.chunks - 1) umma_commit(q_empty);
+                    }
+                    vs_ = nvs;
+                    vp_ = nvp;
                 }
-                if (ok && !issue_pv(sg.chunks - 1, pvst, pvph)) ok = false;
                 for (int h = 0; h < nh; ++h) {
                     gh[h] += sg.chunks;
                     segh[h] += 1;
@@ -490,23 +518,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // -------------- softmax: one warpgroup per half, one row per thread --------------
-        const int h = (warp - 2) >> 2;
+        const int h = (warp - 4) >> 2;
         const int quarter = warp & 3;  // the TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + tl + h * L::HALF_COLS;
-        const uint32_t tO = tmem + tl + h * L::HALF_COLS + L::COL_O;
-        const int tid = threadIdx.x - 64 - 128 * h;  // 0..127 within the warpgroup
+        const uint32_t tO = tS + L::COL_O;
+        const int tid = threadIdx.x - 128 - 128 * h;  // 0..127 within the warpgroup
         const float sl2 = a.scale_log2;
         uint32_t gh = 0;   // chunks this half has processed
         uint32_t gk = 0;   // chunks of the CTA (K/V ring position)
-        int segh = 0;
         bool ok = true;
         for (int64_t f = lo; f < hi && ok;) {
             Segment sg;
-            segment_at(a, pre, f, hi, sg);
+            segment_at<L::BPC>(a, pre, f, hi, sg);
             const UnitPos &u = sg.u;
             if (h == 1 && sg.tile_tokens <= HTOK) {  // this half has no query rows here
                 gk += sg.chunks;
@@ -526,34 +553,40 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 const int nb = min(L::BPC, sg.nblk - L::BPC * ch);
                 const int64_t key0 = (u.kb + (int64_t)L::BPC * ch) * kBS;
                 const int nkeys = nb * kBS;
-                const int bsel = 2 * h + (gh & 1);
-                if (!mbar_wait(&s_full[bsel], (gh >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&s_full[h], gh & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sr[2][32];
-                tmem_ld32(tS + (gh & 1) * L::KT, sr[0]);
-                tmem_ld32(tS + (gh & 1) * L::KT + 32, sr[1]);
-                tmem_wait_ld();
+                // visible keys of this chunk for this row: [0, vis)
                 const int vis = (int)max64(0, min64(lim - key0, (int64_t)nkeys));
-                float v[64];
-                if (__all_sync(0xffffffffu, vis >= 64)) {
+                const bool full = __all_sync(0xffffffffu, vis >= L::KT);
+                // The row's 128 scores in registers, all four loads behind one wait.
+                uint32_t s[L::KT];
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(sr[j >> 5][j & 31]);
-                } else {
+                for (int q = 0; q < L::KT / 32; ++q)
+                    tmem_ld32(tS + q * 32, reinterpret_cast<uint32_t(&)[32]>(s[q * 32]));
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) v[j] = j < vis ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
+                for (int q = 0; q < L::KT / 32; ++q) reg_order32(reinterpret_cast<uint32_t(&)[32]>(s[q * 32]));
+                if (!full) {
+#pragma unroll
+                    for (int j = 0; j < L::KT; ++j)
+                        if (j >= vis) s[j] = __float_as_uint(-INFINITY);
                 }
-                float m4[4] = {v[0], v[1], v[2], v[3]};
+                // row maximum of the raw scores (scale > 0 keeps the order)
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 4; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
-                // raw maximum, then scaled (scale > 0 keeps the order; -inf stays -inf)
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+                for (int j = 0; j < L::KT; j += 8)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        m4[k] = fmax3(m4[k], __uint_as_float(s[j + 2 * k]), __uint_as_float(s[j + 2 * k + 1]));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;  // -inf stays
                 const bool up = mx > m_ref + kRescaleSlack;
                 if (__any_sync(0xffffffffu, up)) {
                     const float alpha = up ? fast_exp2(m_ref - mx) : 1.f;
                     if (ch > 0) {
-                        // O holds this segment's earlier chunks: wait for the last PV, rescale.
+                        // O holds this segment's earlier chunks (PV(c-1) is complete: the
+                        // commit behind this chunk's QK covers it); rescale it.
                         const uint32_t gp = gh - 1;
-                        if (!mbar_wait(&pv_done[2 * h + (gp & 1)], (gp >> 1) & 1, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&pv_done[h], gp & 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int q = 0; q < D / 32; ++q) {
@@ -570,24 +603,34 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (up) m_ref = mx;
                 }
                 const float base = m_ref == -INFINITY ? 0.f : m_ref;
-                // P buffer bsel is free once PV(gh - 2) has read it
-                if (gh >= 2 && !mbar_wait(&pv_done[bsel], ((gh - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-                uint8_t *prow = sP + bsel * L::P_BYTES + row * 128;
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                // weights, written back over S as bf16 pairs: columns [16q, 16q+16) hold keys
+                // [32q, 32q+32) (S was read in full above, so nothing unread is overwritten)
+                // (the row sum adds the fp32 weights, two lanes at a time)
+                const uint64_t sc2 = f2_pack(sl2, sl2), nb2 = f2_pack(-base, -base);
+                uint64_t ps2[2] = {0, 0};
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    uint32_t pk[4];
+                for (int q = 0; q < L::KT / 32; ++q) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 8 * c16 + 2 * e;
-                        pk[e] = pack_bf16x2(fast_exp2(fmaf(v[j], sl2, -base)),
-                                            fast_exp2(fmaf(v[j + 1], sl2, -base)));
-                        ps[e] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                    for (int j = 0; j < 16; ++j) {
+                        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[q * 32 + 2 * j]),
+                                                           __uint_as_float(s[q * 32 + 2 * j + 1])),
+                                                   sc2, nb2);
+                        float x0, x1;
+                        f2_unpack(x2, x0, x1);
+                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                        pk[j] = pack_bf16x2(e0, e1);
+                        ps2[j & 1] = f2_add(ps2[j & 1], f2_pack(e0, e1));
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((c16 ^ (row & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    tmem_st16(tS + q * 16, pk);
                 }
-                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(ps2[0], a0, a1);
+                    f2_unpack(ps2[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
+                tmem_wait_st();
                 if (h == 0 && key0 + nkeys > ctx) {
                     // The chunk runs past the context: the pool rows there may hold NaN, and
                     // 0 * NaN would poison O, so zero those V rows before PV reads them (the
@@ -601,15 +644,15 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                         *reinterpret_cast<uint4 *>(vst + (rem >> 3) * L::KV_DC + rr * 128 + ((rem & 7) << 4)) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
+                    fence_async_smem();
                 }
-                fence_async_smem();
                 tc_fence_before();
-                mbar_arrive(&p_full[bsel]);
+                mbar_arrive(&p_full[h]);
             }
             if (!ok) break;
             // ---- epilogue: O / l for the tile, or the part for the merge ----
             const uint32_t gl = gh - 1;
-            if (!mbar_wait(&pv_done[2 * h + (gl & 1)], (gl >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&pv_done[h], gl & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const bool whole = lo <= u.tile_begin && sg.end == u.tile_begin + u.tile_blocks;
             const float inv = 1.f / l;
@@ -644,7 +687,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             tc_fence_before();
             mbar_arrive(&o_free[h]);
             f = sg.end;
-            ++segh;
         }
         if (!ok) {
             if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
@@ -668,15 +710,15 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     // A tile is two halves of 16 * (8 / group) tokens x group heads (<= 128 rows each).
     p->tokens_per_tile = 2 * 16 * (8 / p->group);
     p->rows = p->tokens_per_tile * p->group;    // <= 256 rows per tile
-    p->warps = 10;  // producer, MMA issuer, one softmax warpgroup per half
+    p->warps = kPrefillThreads / 32;  // producer, MMA issuer, 2 idle, a softmax warpgroup per half
     p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
-    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128, p_bytes = 4 * 128 * 64 * 2;
-    p->stage_bytes = 64 * head_dim * 2;
-    const size_t fixed = 1024 + q_bytes + p_bytes + 8 * 17 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
+    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128;
+    p->stage_bytes = 128 * head_dim * 2;  // K or V of a 128-key chunk
+    const size_t fixed = 1024 + q_bytes + 8 * 11 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
     int nst = (int)(((int64_t)smem_optin - (int64_t)fixed) / (p->stage_bytes + 16));
     if (nst > 8) nst = 8;
-    if (nst < 4) return PKV_ERR_UNSUPPORTED;
+    if (nst < 3) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
     p->smem = fixed + (size_t)nst * (p->stage_bytes + 16);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -691,6 +733,17 @@ template <int D>
 static cudaError_t launch_prefill_d(const CUtensorMap &q_map, const CUtensorMap &k_map,
                                     const CUtensorMap &v_map, const PrefillArgs &a,
                                     const PrefillPlan &p, cudaStream_t stream) {
+    // The register split is only safe when the launch pool covers it.
+    static int regs = -1;
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e0 = cudaFuncGetAttributes(&fa, paged_prefill_kernel<D>);
+        if (e0 != cudaSuccess) return e0;
+        regs = fa.numRegs;
+    }
+    if ((int64_t)regs * kPrefillThreads < 128 * kPrefillRegsLow + 256 * kPrefillRegsHigh ||
+        p.warps * 32 != kPrefillThreads)
+        return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
