@@ -558,26 +558,33 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 // visible keys of this chunk for this row: [0, vis)
                 const int vis = (int)max64(0, min64(lim - key0, (int64_t)nkeys));
                 const bool full = __all_sync(0xffffffffu, vis >= L::KT);
-                // The row's 128 scores in registers, all four loads behind one wait.
-                uint32_t s[L::KT];
+                // Two passes over the row's 128 scores, 64 columns (two loads behind one
+                // wait) at a time: a TMEM round trip costs tens of cycles, while holding all
+                // 128 scores in registers made the compiler spill the loop state.
+                auto load64 = [&](int r, uint32_t (&v)[64]) {
+                    tmem_ld32(tS + r * 64, reinterpret_cast<uint32_t(&)[32]>(v[0]));
+                    tmem_ld32(tS + r * 64 + 32, reinterpret_cast<uint32_t(&)[32]>(v[32]));
+                    tmem_wait_ld();
+                    reg_order32(reinterpret_cast<uint32_t(&)[32]>(v[0]));
+                    reg_order32(reinterpret_cast<uint32_t(&)[32]>(v[32]));
+                    if (!full) {
 #pragma unroll
-                for (int q = 0; q < L::KT / 32; ++q)
-                    tmem_ld32(tS + q * 32, reinterpret_cast<uint32_t(&)[32]>(s[q * 32]));
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < L::KT / 32; ++q) reg_order32(reinterpret_cast<uint32_t(&)[32]>(s[q * 32]));
-                if (!full) {
-#pragma unroll
-                    for (int j = 0; j < L::KT; ++j)
-                        if (j >= vis) s[j] = __float_as_uint(-INFINITY);
-                }
+                        for (int j = 0; j < 64; ++j)
+                            if (r * 64 + j >= vis) v[j] = __float_as_uint(-INFINITY);
+                    }
+                };
                 // row maximum of the raw scores (scale > 0 keeps the order)
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < L::KT; j += 8)
+                for (int r = 0; r < L::KT / 64; ++r) {
+                    uint32_t v[64];
+                    load64(r, v);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        m4[k] = fmax3(m4[k], __uint_as_float(s[j + 2 * k]), __uint_as_float(s[j + 2 * k + 1]));
+                    for (int j = 0; j < 64; j += 8)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            m4[k] = fmax3(m4[k], __uint_as_float(v[j + 2 * k]), __uint_as_float(v[j + 2 * k + 1]));
+                }
                 const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;  // -inf stays
                 const bool up = mx > m_ref + kRescaleSlack;
                 if (__any_sync(0xffffffffu, up)) {
@@ -604,25 +611,30 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 const float base = m_ref == -INFINITY ? 0.f : m_ref;
                 // weights, written back over S as bf16 pairs: columns [16q, 16q+16) hold keys
-                // [32q, 32q+32) (S was read in full above, so nothing unread is overwritten)
-                // (the row sum adds the fp32 weights, two lanes at a time)
+                // [32q, 32q+32), so a round only overwrites columns it has already read; the
+                // row sum adds the fp32 weights, two lanes at a time
                 const uint64_t sc2 = f2_pack(sl2, sl2), nb2 = f2_pack(-base, -base);
                 uint64_t ps2[2] = {0, 0};
 #pragma unroll
-                for (int q = 0; q < L::KT / 32; ++q) {
-                    uint32_t pk[16];
+                for (int r = 0; r < L::KT / 64; ++r) {
+                    uint32_t v[64];
+                    load64(r, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[q * 32 + 2 * j]),
-                                                           __uint_as_float(s[q * 32 + 2 * j + 1])),
-                                                   sc2, nb2);
-                        float x0, x1;
-                        f2_unpack(x2, x0, x1);
-                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-                        pk[j] = pack_bf16x2(e0, e1);
-                        ps2[j & 1] = f2_add(ps2[j & 1], f2_pack(e0, e1));
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(v[q * 32 + 2 * j]),
+                                                               __uint_as_float(v[q * 32 + 2 * j + 1])),
+                                                       sc2, nb2);
+                            float x0, x1;
+                            f2_unpack(x2, x0, x1);
+                            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                            pk[j] = pack_bf16x2(e0, e1);
+                            ps2[j & 1] = f2_add(ps2[j & 1], f2_pack(e0, e1));
+                        }
+                        tmem_st16(tS + (2 * r + q) * 16, pk);
                     }
-                    tmem_st16(tS + q * 16, pk);
                 }
                 {
                     float a0, a1, b0, b1;
