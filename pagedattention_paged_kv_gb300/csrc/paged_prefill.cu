@@ -417,105 +417,119 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         // QK_1(c+1), so one half's MMAs run while the other half's softmax works.  QK_h(c+1)
         // overwrites S_h right after PV_h(c) read P_h from it; MMAs of one thread run in issue
         // order, and the softmax learns both are done from the commit behind QK_h(c+1).
-        if (lane == 0) {
-            const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dk0 = umma_desc_sw128(smem_u32(sStage), 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(smem_u32(sStage), L::KV_DC, 1024);
-            constexpr uint32_t STG16 = L::STG >> 4;
-            uint32_t kst = 0, kph = 0;  // ring slot of the next chunk's K
-            uint32_t gh[2] = {0, 0};    // chunks each half has processed
-            int segh[2] = {0, 0};       // segments each half has processed
-            int seg_i = 0;
-            bool ok = true;
-            bool issued = false;
-            auto adv = [&](uint32_t &st, uint32_t &ph) {
-                if (++st == (uint32_t)NST) { st = 0; ph ^= 1; }
-            };
-            auto issue_qk = [&](int h, uint32_t kslot) {
-                const uint64_t dk = dk0 + kslot * STG16;
-                const uint64_t dq = dq0 + h * (L::HALF_DC >> 4);
-                const uint32_t tS = tmem + h * L::HALF_COLS;
+        // The whole warp runs this loop on warp-uniform values and one elected lane issues
+        // (the same lane every time, so each commit covers every MMA before it); waits end
+        // together for the warp (a timeout seen by any lane aborts all of them).
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+        };
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        const uint64_t dq0 = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk0 = umma_desc_sw128(smem_u32(sStage), 16, 1024);
+        const uint64_t dv0 = umma_desc_sw128(smem_u32(sStage), L::KV_DC, 1024);
+        constexpr uint32_t STG16 = L::STG >> 4;
+        uint32_t kst = 0, kph = 0;  // ring slot of the next chunk's K
+        uint32_t gh[2] = {0, 0};    // chunks each half has processed
+        int segh[2] = {0, 0};       // segments each half has processed
+        int seg_i = 0;
+        bool ok = true;
+        bool issued = false;
+        auto adv = [&](uint32_t &st, uint32_t &ph) {
+            if (++st == (uint32_t)NST) { st = 0; ph ^= 1; }
+        };
+        auto issue_qk = [&](int h, uint32_t kslot) {
+            const uint64_t dk = dk0 + kslot * STG16;
+            const uint64_t dq = dq0 + h * (L::HALF_DC >> 4);
+            const uint32_t tS = tm + h * L::HALF_COLS;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = ((ks / 4) * L::KV_DC + (ks % 4) * 32) >> 4;
-                    const uint32_t qoff = ((ks / 4) * L::Q_DC + (ks % 4) * 32) >> 4;
-                    umma_bf16(tS, dq + qoff, dk + koff, IDESC_QK, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t koff = ((ks / 4) * L::KV_DC + (ks % 4) * 32) >> 4;
+                const uint32_t qoff = ((ks / 4) * L::Q_DC + (ks % 4) * 32) >> 4;
+                umma_bf16_warp(tS, dq + qoff, dk + koff, IDESC_QK, ks > 0);
+            }
+            umma_commit_warp(&s_full[h]);
+            issued = true;
+        };
+        for (int64_t f = lo; f < hi && ok;) {
+            Segment sg;
+            segment_at<L::BPC>(a, pre, f, hi, sg);
+            const int chunks = __shfl_sync(0xffffffffu, sg.chunks, 0);
+            const int nh = __shfl_sync(0xffffffffu, sg.tile_tokens > HTOK ? 2 : 1, 0);  // halves with rows
+            if (!wait_all(q_full, seg_i & 1)) { ok = false; break; }
+            // chunk 0's K and V slots
+            uint32_t ks_ = kst, kp_ = kph;
+            uint32_t vs_ = kst, vp_ = kph;
+            adv(vs_, vp_);
+            kst = vs_;
+            kph = vp_;
+            adv(kst, kph);
+            if (!wait_all(&kv_full[ks_], kp_)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (h < nh) issue_qk(h, ks_);
+            umma_commit_warp(&kv_empty[ks_]);
+            if (chunks == 1) umma_commit_warp(q_empty);
+            for (int ch = 0; ch < chunks && ok; ++ch) {
+                const bool more = ch + 1 < chunks;
+                uint32_t nks = kst, nkp = kph;  // the next chunk's K and V slots
+                uint32_t nvs = kst, nvp = kph;
+                if (more) {
+                    adv(nvs, nvp);
+                    kst = nvs;
+                    kph = nvp;
+                    adv(kst, kph);
                 }
-                umma_commit(&s_full[h]);
-                issued = true;
-            };
-            for (int64_t f = lo; f < hi && ok;) {
-                Segment sg;
-                segment_at<L::BPC>(a, pre, f, hi, sg);
-                const int nh = sg.tile_tokens > HTOK ? 2 : 1;  // halves with query rows
-                if (!mbar_wait(q_full, seg_i & 1, abort_flag)) { ok = false; break; }
-                // chunk 0's K and V slots
-                uint32_t ks_ = kst, kp_ = kph;
-                uint32_t vs_ = kst, vp_ = kph;
-                adv(vs_, vp_);
-                kst = vs_;
-                kph = vp_;
-                adv(kst, kph);
-                if (!mbar_wait(&kv_full[ks_], kp_, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                for (int h = 0; h < nh; ++h) issue_qk(h, ks_);
-                umma_commit(&kv_empty[ks_]);
-                if (sg.chunks == 1) umma_commit(q_empty);
-                for (int ch = 0; ch < sg.chunks && ok; ++ch) {
-                    const bool more = ch + 1 < sg.chunks;
-                    uint32_t nks = kst, nkp = kph;  // the next chunk's K and V slots
-                    uint32_t nvs = kst, nvp = kph;
-                    if (more) {
-                        adv(nvs, nvp);
-                        kst = nvs;
-                        kph = nvp;
-                        adv(kst, kph);
+                if (!wait_all(&kv_full[vs_], vp_)) { ok = false; break; }
+                const uint64_t dv = dv0 + vs_ * STG16;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h >= nh) break;
+                    const uint32_t gg = gh[h] + ch;
+                    if (ch == 0 && segh[h] > 0 && !wait_all(&o_free[h], (segh[h] - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
-                    if (!mbar_wait(&kv_full[vs_], vp_, abort_flag)) { ok = false; break; }
-                    if (more && !mbar_wait(&kv_full[nks], nkp, abort_flag)) { ok = false; break; }
-                    const uint64_t dv = dv0 + vs_ * STG16;
-                    for (int h = 0; h < nh && ok; ++h) {
-                        const uint32_t gg = gh[h] + ch;
-                        if (ch == 0 && segh[h] > 0 && !mbar_wait(&o_free[h], (segh[h] - 1) & 1, abort_flag)) {
-                            ok = false;
-                            break;
+                    if (!wait_all(&p_full[h], gg & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t tP = tm + h * L::HALF_COLS;
+                    const uint32_t tO = tP + L::COL_O;
+#pragma unroll
+                    for (int ks = 0; ks < L::KT / 16; ++ks)
+                        umma_bf16_tmem_a_warp(tO, tP + ks * 8, dv + ks * (2048 >> 4), IDESC_PV,
+                                              !(ch == 0 && ks == 0));
+                    umma_commit_warp(&pv_done[h]);
+                    if (h == nh - 1) umma_commit_warp(&kv_empty[vs_]);  // V(c) read by every half
+                    if (more) {
+                        if (h == 0 && !wait_all(&kv_full[nks], nkp)) { ok = false; break; }
+                        issue_qk(h, nks);
+                        if (h == nh - 1) {
+                            umma_commit_warp(&kv_empty[nks]);
+                            if (ch + 1 == chunks - 1) umma_commit_warp(q_empty);
                         }
-                        if (!mbar_wait(&p_full[h], gg & 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t tP = tmem + h * L::HALF_COLS;
-                        const uint32_t tO = tP + L::COL_O;
-#pragma unroll
-                        for (int ks = 0; ks < L::KT / 16; ++ks)
-                            umma_bf16_tmem_a(tO, tP + ks * 8, dv + ks * (2048 >> 4), IDESC_PV,
-                                             !(ch == 0 && ks == 0));
-                        umma_commit(&pv_done[h]);
-                        if (more) issue_qk(h, nks);
                     }
-                    if (!ok) break;
-                    umma_commit(&kv_empty[vs_]);
-                    if (more) {
-                        umma_commit(&kv_empty[nks]);
-                        if (ch + 1 == sg.chunks - 1) umma_commit(q_empty);
-                    }
-                    vs_ = nvs;
-                    vp_ = nvp;
                 }
-                for (int h = 0; h < nh; ++h) {
-                    gh[h] += sg.chunks;
+                if (!ok) break;
+                vs_ = nvs;
+                vp_ = nvp;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (h < nh) {
+                    gh[h] += chunks;
                     segh[h] += 1;
                 }
-                f = sg.end;
-                ++seg_i;
-            }
-            if (!ok) {
-                flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            // every MMA this thread issued is finished before TMEM is released
-            if (issued) {
-                umma_commit(mma_done);
-                mbar_wait(mma_done, 0, nullptr);
-            }
+            f = sg.end;
+            ++seg_i;
+        }
+        if (!ok) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        // every MMA the warp issued is finished before TMEM is released
+        if (issued) {
+            umma_commit_warp(mma_done);
+            mbar_wait(mma_done, 0, nullptr);
         }
         __syncwarp();
     } else if (warp >= 4) {
