@@ -232,7 +232,11 @@ struct PrefillSmem {
     static constexpr uint32_t Q_BYTES = (D / 64) * Q_DC;
     static constexpr uint32_t KV_DC = KT * 128;                // 128 keys x 64 columns
     static constexpr uint32_t STG = (D / 64) * KV_DC;          // K or V of one chunk
-    static constexpr uint32_t OFF_STAGES = Q_BYTES;
+    // Epilogue staging: 4 KiB per softmax warp (32 rows x 128 bytes), so O leaves in
+    // whole 128-byte lines instead of one row per thread.
+    static constexpr uint32_t EPI_WARP = 4096;
+    static constexpr uint32_t OFF_EPI = Q_BYTES;
+    static constexpr uint32_t OFF_STAGES = Q_BYTES + 8 * EPI_WARP;
     // TMEM, per half: S (128 fp32 columns; P overwrites its first 64 as bf16 pairs), O.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t HALF_COLS = 256;
@@ -273,7 +277,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = a.num_stages;
-    uint8_t *sQ = smem, *sStage = smem + L::OFF_STAGES;
+    uint8_t *sQ = smem, *sStage = smem + L::OFF_STAGES, *sEpi = smem + L::OFF_EPI;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)NST * L::STG);
     // per half h: s_full[h], p_full[h], pv_done[h], o_free[h]
     uint64_t *q_full = bars, *q_empty = bars + 1, *mma_done = bars + 2;
@@ -589,7 +593,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 };
                 // row maximum of the raw scores (scale > 0 keeps the order)
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+#pragma unroll 1
                 for (int r = 0; r < L::KT / 64; ++r) {
                     uint32_t v[64];
                     load64(r, v);
@@ -629,7 +633,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                 // row sum adds the fp32 weights, two lanes at a time
                 const uint64_t sc2 = f2_pack(sl2, sl2), nb2 = f2_pack(-base, -base);
                 uint64_t ps2[2] = {0, 0};
-#pragma unroll
+#pragma unroll 1
                 for (int r = 0; r < L::KT / 64; ++r) {
                     uint32_t v[64];
                     load64(r, v);
@@ -682,31 +686,70 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             tc_fence_after();
             const bool whole = lo <= u.tile_begin && sg.end == u.tile_begin + u.tile_blocks;
             const float inv = 1.f / l;
-            const int64_t qrow = u.t.q_row0 + u.qt * TPT + tok;
-            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)u.kvh * group + hg) * D;
             const int slot = whole ? 0 : part_slot(c, u.tile_begin, T, ge);
             const int trow = tok * group + hg;  // row inside the tile
-            float *wrow = a.ws_o + ((int64_t)slot * tile_rows + trow) * D;
+            // Staged through this warp's 32 x 128-byte buffer: each lane writes its row's
+            // 128 bytes (16-byte chunks XOR-swizzled by row, so a store instruction touches
+            // every bank once), then lane l reads chunk l % 8 of row 4k + l / 8 and stores it,
+            // so each store instruction writes 4 whole 128-byte lines.
+            uint8_t *ebuf = sEpi + (size_t)(warp - 4) * L::EPI_WARP;
+            const int er = lane >> 3, ec = lane & 7;
+            auto stage_and_store = [&](const uint32_t (&v)[32], auto &&dst_of_row) {
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t r[32];
-                tmem_ld32(tO + q * 32, r);
-                tmem_wait_ld();
-                if (!rvalid) continue;
-                if (whole) {
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(ebuf + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                        make_uint4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-                        o.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-                        o.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-                        o.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + q * 32 + j) = o;
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + er;  // row within the warp
+                    const uint4 x = *reinterpret_cast<const uint4 *>(ebuf + rr * 128 + ((ec ^ (rr & 7)) << 4));
+                    uint8_t *dst = dst_of_row(quarter * 32 + rr);
+                    if (dst) *reinterpret_cast<uint4 *>(dst + ec * 16) = x;
+                }
+                __syncwarp();
+            };
+            // global address of a half row's 128-byte piece, or null for rows with no query
+            auto row_ok = [&](int hr, int &tk, int &hgr) {
+                tk = hr / group;
+                hgr = hr - tk * group;
+                return hr < half_rows && tk < half_tokens;
+            };
+            if (whole) {
+#pragma unroll 1
+                for (int hb = 0; hb < D / 64; ++hb) {  // 64 columns = 128 bytes of bf16
+                    uint32_t r0[32], r1[32], v[32];
+                    tmem_ld32(tO + hb * 64, r0);
+                    tmem_ld32(tO + hb * 64 + 32, r1);
+                    tmem_wait_ld();
+                    reg_order32(r0);
+                    reg_order32(r1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        v[j] = pack_bf16x2(__uint_as_float(r0[2 * j]) * inv, __uint_as_float(r0[2 * j + 1]) * inv);
+                        v[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]) * inv, __uint_as_float(r1[2 * j + 1]) * inv);
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<uint4 *>(wrow + q * 32 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                    stage_and_store(v, [&](int hr) -> uint8_t * {
+                        int tk, hgr;
+                        if (!row_ok(hr, tk, hgr)) return nullptr;
+                        const int64_t qr = u.t.q_row0 + u.qt * TPT + h * HTOK + tk;
+                        return reinterpret_cast<uint8_t *>(
+                                   a.out + (qr * a.num_heads + (int64_t)u.kvh * group + hgr) * D) + hb * 128;
+                    });
+                }
+            } else {
+#pragma unroll 1
+                for (int q = 0; q < D / 32; ++q) {  // 32 fp32 columns = 128 bytes
+                    uint32_t v[32];
+                    tmem_ld32(tO + q * 32, v);
+                    tmem_wait_ld();
+                    reg_order32(v);
+                    stage_and_store(v, [&](int hr) -> uint8_t * {
+                        int tk, hgr;
+                        if (!row_ok(hr, tk, hgr)) return nullptr;
+                        const int tr = (h * HTOK + tk) * group + hgr;
+                        return reinterpret_cast<uint8_t *>(a.ws_o + ((int64_t)slot * tile_rows + tr) * D) + q * 128;
+                    });
                 }
             }
             if (!whole && rvalid) a.ws_ml[(int64_t)slot * tile_rows + trow] = make_float2(m_ref, l);
@@ -739,7 +782,7 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     p->warps = kPrefillThreads / 32;  // producer, MMA issuer, 2 idle, a softmax warpgroup per half
     p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
-    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128;
+    const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128 + 8 * 4096;  // Q + epilogue staging
     p->stage_bytes = 128 * head_dim * 2;  // K or V of a 128-key chunk
     const size_t fixed = 1024 + q_bytes + 8 * 11 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
     int nst = (int)(((int64_t)smem_optin - (int64_t)fixed) / (p->stage_bytes + 16));
