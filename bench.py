@@ -185,15 +185,19 @@ DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "pkv_
                   "pkv_split.cuh", "merge.cuh")
 
 
-def recorded_traffic(name, sources):
+PREFILL_SOURCES = ("paged_prefill.cu", "paged_prefill.cuh", "tcgen05.cuh", "fp32x2.cuh", "attn_block.cuh",
+                   "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
+
+
+def recorded_traffic(name, sources, config):
     """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    current kernel source and on this bench configuration (else None)."""
     path = os.path.join(ROOT, "profiles", f"{name}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("source_sha") != kernel_source_sha(sources):
+    if d.get("source_sha") != kernel_source_sha(sources) or d.get("bench_config") != config:
         return None
     return d
 
@@ -485,7 +489,7 @@ def main():
     # ---- varlen only: the chunk alone and the decodes alone ----
     parts = None
     if varlen:
-        parts = varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak)
+        parts = varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, args.config)
 
     if rank != 0:
         return
@@ -511,7 +515,7 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if not varlen:
-        traffic = recorded_traffic("decode", DECODE_SOURCES)
+        traffic = recorded_traffic("decode", DECODE_SOURCES, args.config)
         achieved = attn_bytes / (t_attn * 1e-3) / 1e9
         line["roofline"] = {
             "bound": "hbm", "kernel": "paged_decode_kernel (+ merge_parts_kernel, timed together)",
@@ -530,7 +534,7 @@ def main():
     print(json.dumps(line), flush=True)
 
 
-def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak):
+def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
     """Times the chunk rows alone and the decode rows alone (same pool, same call)."""
     res = {}
     ql = b.q_lens
@@ -568,9 +572,11 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak):
             tf = fl / (t * 1e-3) / 1e12
             res["chunk_us"] = t * 1e3
             res["chunk_tflops"] = tf
+            traffic = recorded_traffic("prefill", PREFILL_SOURCES, config)
             res["roofline"] = {"bound": "tensor", "kernel": "paged_prefill_kernel (+ merge, timed together)",
                                "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
-                               "peak_source": "measured bf16_tflops (burst cuBLAS)", "traffic": None,
+                               "peak_source": "measured bf16_tflops (burst cuBLAS)",
+                               "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                                "algorithmic_flops": fl}
         else:
             byts = int(b.context_lens[seqs].astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 4

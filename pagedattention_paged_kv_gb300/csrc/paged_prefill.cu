@@ -28,6 +28,7 @@
 //    64-column slice) into a ring of shared-memory stages.
 //  * Waits are bounded in time; no CTA waits on another CTA.
 #include "attn_block.cuh"
+#include "fp32x2.cuh"
 #include "merge.cuh"
 #include "paged_prefill.cuh"
 #include "pkv_split.cuh"
