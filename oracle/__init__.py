@@ -58,6 +58,16 @@ class Oracle:
         lib.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                i32, i64, dbl, i32, vp]
         lib.oracle_paged_attention.restype = i32
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = dbl
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                                     ctypes.c_float, ctypes.c_float]
+        lib.oracle_reshape_and_cache_fp8.restype = i32
+        lib.oracle_paged_attention_fp8.argtypes = [vp, vp, vp, vp, dbl, dbl, vp, vp, vp, i64, i64, i32,
+                                                   i32, i32, i32, i64, dbl, i32, vp]
+        lib.oracle_paged_attention_fp8.restype = i32
         self.lib = lib
 
     # -- threads ---------------------------------------------------------------
@@ -112,6 +122,50 @@ class Oracle:
             int(bool(causal)), _p(rm))
         if rc != 0:
             raise ValueError("oracle_paged_attention: invalid input")
+        return out
+
+
+    # -- FP8 (OCP e4m3) cache ---------------------------------------------------
+    def e4m3_decode(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_decode(int(code) & 0xFF))
+
+    def e4m3_encode(self, y: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(y)))
+
+    def reshape_and_cache_fp8(self, k_cache, v_cache, k, v, slot_mapping, k_scale: float,
+                              v_scale: float) -> None:
+        """Writes e4m3 codes into k_cache/v_cache (uint8 [NB, bs, Hkv, d]) in place."""
+        assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous
+        assert v_cache.dtype == np.uint8 and v_cache.flags.c_contiguous
+        NB, bs, Hkv, d = k_cache.shape
+        kk = np.ascontiguousarray(k, dtype=np.uint16)
+        vv = np.ascontiguousarray(v, dtype=np.uint16)
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        rc = self.lib.oracle_reshape_and_cache_fp8(_p(k_cache), _p(v_cache), _p(kk), _p(vv), _p(sm),
+                                                   sm.shape[0], NB, bs, Hkv, d, float(k_scale),
+                                                   float(v_scale))
+        if rc != 0:
+            raise ValueError("oracle_reshape_and_cache_fp8: slot outside the pool or bad scale")
+
+    def paged_attention_fp8(self, q, k_cache, v_cache, k_scale: float, v_scale: float, block_tables,
+                            context_lens, scale: float, query_start_loc=None, causal: bool = True,
+                            row_mask=None) -> np.ndarray:
+        """Attention over an e4m3 cache (uint8 codes); fp64 [total_q, Hq, d]."""
+        qq = np.ascontiguousarray(q, dtype=np.uint16)
+        total_q, Hq, d = qq.shape
+        NB, bs, Hkv, d2 = k_cache.shape
+        assert d2 == d and k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        qsl = None if query_start_loc is None else np.ascontiguousarray(query_start_loc, np.int32)
+        rm = None if row_mask is None else np.ascontiguousarray(row_mask, dtype=np.uint8)
+        out = np.full((total_q, Hq, d), np.nan, dtype=np.float64)
+        rc = self.lib.oracle_paged_attention_fp8(
+            _p(out), _p(qq), _p(np.ascontiguousarray(k_cache)), _p(np.ascontiguousarray(v_cache)),
+            float(k_scale), float(v_scale), _p(bt), _p(cl), _p(qsl), cl.shape[0], bt.shape[1], Hq, Hkv,
+            d, bs, NB, float(scale), int(bool(causal)), _p(rm))
+        if rc != 0:
+            raise ValueError("oracle_paged_attention_fp8: invalid input")
         return out
 
 

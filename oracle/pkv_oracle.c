@@ -36,7 +36,13 @@
  *   - context_lens counts this step's new tokens, which the KV write stores first;
  *   - the q_len rows of a sequence sit at the last q_len positions of its context;
  *     with causal masking row j sees keys 0 .. context_len - q_len + j;
- *   - a sequence with context_len 0 gets an all-zero output.
+ *   - a sequence with context_len 0 gets an all-zero output;
+ *   - an FP8 cache (the pages' headline model runs in FP8: [LESSON], the Llama 3.3
+ *     70B FP8 serving numbers) holds OCP e4m3 codes with one scale for K and one for
+ *     V: a cached element means code_value * scale; a new element is stored as the
+ *     e4m3 code nearest to fp32(x) / scale (one correctly rounded fp32 division),
+ *     ties to the even code, magnitudes beyond the largest finite code (448) clamped
+ *     to it.
  */
 #include <math.h>
 #include <stdint.h>
@@ -55,6 +61,47 @@ static double bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * OCP 8-bit floating point, E4M3 variant: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits.  Exponent field 0 is subnormal (m * 2^-9); exponent field 15 with
+ * mantissa 7 is NaN; there are no infinities, so the largest finite value is
+ * 1.75 * 2^8 = 448 (code 0x7E).
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * The e4m3 code nearest to y: a plain search over the 127 non-negative finite codes
+ * (their values increase with the code), ties to the even code; |y| > 448 gives 448;
+ * NaN gives 0x7F.  The sign bit is copied (-0.0 -> 0x80).
+ */
+uint8_t oracle_e4m3_encode(float y)
+{
+    if (isnan(y)) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (a > 448.0) a = 448.0;
+    int best = 0;
+    double best_err = a;  /* code 0 has value 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
 }
 
 int oracle_num_threads(void)
@@ -135,6 +182,43 @@ int oracle_reshape_and_cache(uint16_t *k_cache, uint16_t *v_cache, const uint16_
     return status;
 }
 
+/*
+ * FP8 KV write: the same placement as above; each element is stored as
+ * e4m3(fp32(x) / scale) with x the bf16 value, k_scale for K and v_scale for V.
+ */
+int oracle_reshape_and_cache_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k,
+                                 const uint16_t *v, const int64_t *slot_mapping,
+                                 int64_t num_tokens, int64_t num_blocks, int block_size,
+                                 int num_kv_heads, int head_dim, float k_scale, float v_scale)
+{
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f)) return -1;
+    int status = 0;
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) {
+            status = -1;
+            continue;
+        }
+        const int64_t block = slot / block_size;
+        const int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int e = 0; e < head_dim; ++e) {
+                int64_t dst = ((block * block_size + offset) * num_kv_heads + h) * head_dim + e;
+                int64_t src = t * row + (int64_t)h * head_dim + e;
+                float xk = (float)bf16_to_double(k[src]);
+                float xv = (float)bf16_to_double(v[src]);
+                float yk = xk / k_scale;
+                float yv = xv / v_scale;
+                k_cache[dst] = oracle_e4m3_encode(yk);
+                v_cache[dst] = oracle_e4m3_encode(yv);
+            }
+        }
+    }
+    return status;
+}
+
 /* Check the inputs that decide which memory the attention reads. */
 static int check_sequence(const int32_t *block_tables, int64_t max_blocks_per_seq,
                           int64_t num_blocks, int block_size, int64_t s, int64_t ctx,
@@ -158,8 +242,9 @@ static int check_sequence(const int32_t *block_tables, int64_t max_blocks_per_se
  *     the keys it may see, w_i = exp(z_i - max z), out = sum_i w_i V_i / sum_i w_i
  *     (textbook softmax(q K^T scale) V).
  */
-static void attend_one(double *out, const uint16_t *q, const uint16_t *k_cache,
-                       const uint16_t *v_cache, const int32_t *block_tables,
+static void attend_one(double *out, const uint16_t *q, const void *k_cache,
+                       const void *v_cache, int fp8, double k_scale, double v_scale,
+                       const int32_t *block_tables,
                        int64_t max_blocks_per_seq, int num_heads, int num_kv_heads, int head_dim,
                        int block_size, double scale, int causal, int64_t s, int h, int64_t ctx,
                        int64_t row0, int64_t q_len, const uint8_t *row_mask)
@@ -177,8 +262,13 @@ static void attend_one(double *out, const uint16_t *q, const uint16_t *k_cache,
         int64_t offset = p % block_size;
         for (int e = 0; e < head_dim; ++e) {
             int64_t src = ((physical * block_size + offset) * num_kv_heads + hk) * head_dim + e;
-            K[p * head_dim + e] = bf16_to_double(k_cache[src]);
-            V[p * head_dim + e] = bf16_to_double(v_cache[src]);
+            if (fp8) {
+                K[p * head_dim + e] = oracle_e4m3_decode(((const uint8_t *)k_cache)[src]) * k_scale;
+                V[p * head_dim + e] = oracle_e4m3_decode(((const uint8_t *)v_cache)[src]) * v_scale;
+            } else {
+                K[p * head_dim + e] = bf16_to_double(((const uint16_t *)k_cache)[src]);
+                V[p * head_dim + e] = bf16_to_double(((const uint16_t *)v_cache)[src]);
+            }
         }
     }
 
@@ -218,12 +308,12 @@ static void attend_one(double *out, const uint16_t *q, const uint16_t *k_cache,
     free(qd);
 }
 
-int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
-                           const uint16_t *v_cache, const int32_t *block_tables,
-                           const int32_t *context_lens, const int32_t *query_start_loc,
-                           int64_t num_seqs, int64_t max_blocks_per_seq, int num_heads,
-                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                           double scale, int causal, const uint8_t *row_mask)
+static int attention(double *out, const uint16_t *q, const void *k_cache, const void *v_cache,
+                     int fp8, double k_scale, double v_scale, const int32_t *block_tables,
+                     const int32_t *context_lens, const int32_t *query_start_loc,
+                     int64_t num_seqs, int64_t max_blocks_per_seq, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                     double scale, int causal, const uint8_t *row_mask)
 {
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
     if (head_dim <= 0 || block_size <= 0) return -1;
@@ -242,9 +332,37 @@ int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cac
         int h = (int)(u % num_heads);
         int64_t row0 = query_start_loc ? query_start_loc[s] : s;
         int64_t q_len = query_start_loc ? query_start_loc[s + 1] - query_start_loc[s] : 1;
-        attend_one(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_heads,
+        attend_one(out, q, k_cache, v_cache, fp8, k_scale, v_scale, block_tables,
+                   max_blocks_per_seq, num_heads,
                    num_kv_heads, head_dim, block_size, scale, causal, s, h, context_lens[s], row0,
                    q_len, row_mask);
     }
     return 0;
+}
+
+int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, const int32_t *query_start_loc,
+                           int64_t num_seqs, int64_t max_blocks_per_seq, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           double scale, int causal, const uint8_t *row_mask)
+{
+    return attention(out, q, k_cache, v_cache, 0, 1.0, 1.0, block_tables, context_lens,
+                     query_start_loc, num_seqs, max_blocks_per_seq, num_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, causal, row_mask);
+}
+
+/* The same attention over an FP8 cache: element = e4m3 value of the code * scale. */
+int oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, double k_scale, double v_scale,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               const int32_t *query_start_loc, int64_t num_seqs,
+                               int64_t max_blocks_per_seq, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, double scale,
+                               int causal, const uint8_t *row_mask)
+{
+    if (!(k_scale > 0.0) || !(v_scale > 0.0)) return -1;
+    return attention(out, q, k_cache, v_cache, 1, k_scale, v_scale, block_tables, context_lens,
+                     query_start_loc, num_seqs, max_blocks_per_seq, num_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, causal, row_mask);
 }

@@ -40,6 +40,24 @@ int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cac
                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                            double scale, int causal, const uint8_t *row_mask);
 
+/* FP8 (OCP e4m3) cache: k_cache, v_cache hold one code byte per element.  The codec
+ * functions are exported for the tests. */
+double oracle_e4m3_decode(uint8_t code);
+uint8_t oracle_e4m3_encode(float y);
+
+int oracle_reshape_and_cache_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k,
+                                 const uint16_t *v, const int64_t *slot_mapping,
+                                 int64_t num_tokens, int64_t num_blocks, int block_size,
+                                 int num_kv_heads, int head_dim, float k_scale, float v_scale);
+
+int oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, double k_scale, double v_scale,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               const int32_t *query_start_loc, int64_t num_seqs,
+                               int64_t max_blocks_per_seq, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, double scale,
+                               int causal, const uint8_t *row_mask);
+
 #ifdef __cplusplus
 }
 #endif

@@ -7,6 +7,8 @@ oracle disagrees.  ``test_oracle_pins.py`` runs them on the oracle;
 requires each copy to fail at least one pin.
 
 Sources:
+  [OCP8]   OCP 8-bit Floating Point Specification (OFP8), format E4M3 -- the element
+           type of the FP8 cache (the pages' headline model runs in FP8).
   [LPNH]   "vLLM推理引擎架构PagedAttention机制与高吞吐推理" (lpnh.cn), §2.2 BlockManager
            (pool layout), §2.3 PagedAttention Kernel (arguments and semantics).
   [LESSON] "Servis Motor İçleri: PagedAttention, Sürekli Batching, parçalanmış Prefill"
@@ -377,6 +379,127 @@ def pin_chunking_is_invisible(orc):
                                 query_start_loc=np.array([0, hi - lo], np.int32))
         rows.append(o)
     assert np.array_equal(np.concatenate(rows), whole)
+
+
+# ---------------------------------------------------------------------------
+# FP8 cache (OCP 8-bit floating point, E4M3): the format's definition and
+# torch's float8_e4m3fn type (a library implementation of the same format)
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_values(codes):
+    t = torch.from_numpy(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def pin_e4m3_codes_fixed_by_the_format(orc):
+    """Values the E4M3 definition fixes: bias 7, three mantissa bits, subnormals
+    m * 2^-9 at exponent 0, largest finite 448, NaN at S.1111.111, no infinities."""
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0, 0xB8: -1.0,
+             0xFE: -448.0}
+    for c, v in known.items():
+        assert orc.e4m3_decode(c) == v, (hex(c), orc.e4m3_decode(c), v)
+    assert math.copysign(1.0, orc.e4m3_decode(0x80)) == -1.0 and orc.e4m3_decode(0x80) == 0.0
+    assert math.isnan(orc.e4m3_decode(0x7F)) and math.isnan(orc.e4m3_decode(0xFF))
+
+
+def pin_e4m3_decode_matches_torch(orc):
+    """Every finite code decodes to torch's float8_e4m3fn value."""
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    ref = _torch_e4m3_values(codes)
+    got = np.array([orc.e4m3_decode(c) for c in codes])
+    assert np.array_equal(got, ref)
+
+
+def pin_e4m3_encode_round_to_nearest_even(orc):
+    """Encoding: exact values keep their code; a value halfway between two
+    neighbouring codes takes the even one; magnitudes past 448 saturate; other
+    in-range values agree with torch's float8_e4m3fn cast."""
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert orc.e4m3_encode(orc.e4m3_decode(c)) == c, hex(c)
+    for c in range(0, 0x7E):
+        lo, hi = orc.e4m3_decode(c), orc.e4m3_decode(c + 1)
+        mid = (lo + hi) / 2  # exact in float32 (at most 5 significant bits)
+        want = c if c % 2 == 0 else c + 1
+        assert orc.e4m3_encode(mid) == want, (hex(c), mid)
+        assert orc.e4m3_encode(-mid) == want | 0x80
+    for y in (448.5, 460.0, 480.0, 1e6, 3.0e38):
+        assert orc.e4m3_encode(y) == 0x7E and orc.e4m3_encode(-y) == 0xFE
+    rng = _rng(91)
+    ys = (rng.standard_normal(4000) * np.exp2(rng.uniform(-12, 8, 4000))).astype(np.float32)
+    ys = ys[np.abs(ys) <= 448]
+    ref = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(y)) for y in ys], dtype=np.uint8)
+    assert np.array_equal(got, ref), int(np.count_nonzero(got != ref))
+
+
+def pin_fp8_write_places_and_quantises(orc):
+    """FP8 KV write: the same slots as the bf16 write; with a power-of-two scale,
+    a value that is exactly (e4m3 value x scale) is stored as that code, and an
+    N(0,1) value x is stored as torch's e4m3 cast of x / scale (exact division)."""
+    rng = _rng(92)
+    NB, bs, Hkv, d = 6, 16, 2, 8
+    T = 9
+    slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+    slots[3] = -1  # padding token
+    codes_k = rng.integers(0, 0x7E, size=(T, Hkv, d)) | (rng.integers(0, 2, size=(T, Hkv, d)) << 7)
+    k_scale, v_scale = 2.0 ** -6, 2.0 ** -5
+    kx = np.array([orc.e4m3_decode(int(c)) for c in codes_k.ravel()]).reshape(codes_k.shape) * k_scale
+    k = bf16_bits(kx.astype(np.float32))
+    assert np.array_equal(bf16_to_f32(k).astype(np.float64), kx)  # exactly representable
+    v = normal_bf16(rng, (T, Hkv, d))
+    kc = np.full((NB, bs, Hkv, d), 0x7F, np.uint8)
+    vc = np.full((NB, bs, Hkv, d), 0x7F, np.uint8)
+    orc.reshape_and_cache_fp8(kc, vc, k, v, slots, k_scale, v_scale)
+    v_ref = torch.from_numpy(bf16_to_f32(v) / np.float32(v_scale)).to(torch.float8_e4m3fn)
+    v_ref = v_ref.view(torch.uint8).numpy()
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        b, o = divmod(int(slots[t]), bs)
+        assert np.array_equal(kc[b, o], codes_k[t].astype(np.uint8)), t
+        assert np.array_equal(vc[b, o], v_ref[t]), t
+    written = np.zeros((NB, bs), bool)
+    for t in range(T):
+        if slots[t] >= 0:
+            written[divmod(int(slots[t]), bs)] = True
+    assert np.all(kc[~written] == 0x7F) and np.all(vc[~written] == 0x7F)
+
+
+def pin_fp8_attention_equals_dequantised_bf16(orc):
+    """Attention over an e4m3 pool equals attention over the bf16 pool holding the
+    dequantised values (code value x scale, exact in bf16 for power-of-two scales),
+    which the bf16 pins tie to torch's SDPA.  Unused slots hold the NaN code."""
+    rng = _rng(93)
+    ctx = [1, 16, 17, 40, 70]
+    Hq, Hkv, d, bs = 8, 2, 16, 16
+    nblk = [-(-c // bs) for c in ctx]
+    NB = sum(nblk) + 2
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((len(ctx), max(nblk)), -1, np.int32)
+    at = 0
+    for s, n in enumerate(nblk):
+        tables[s, :n] = perm[at:at + n]
+        at += n
+    kc = np.full((NB, bs, Hkv, d), 0x7F, np.uint8)
+    vc = np.full((NB, bs, Hkv, d), 0x7F, np.uint8)
+    for s, c in enumerate(ctx):
+        for i in range(nblk[s]):
+            n = min(bs, c - i * bs)
+            kc[tables[s, i], :n] = rng.integers(0, 0x7E, size=(n, Hkv, d)) | (rng.integers(0, 2, size=(n, Hkv, d)) << 7)
+            vc[tables[s, i], :n] = rng.integers(0, 0x7E, size=(n, Hkv, d)) | (rng.integers(0, 2, size=(n, Hkv, d)) << 7)
+    k_scale, v_scale = 2.0 ** -7, 2.0 ** -4
+    lut = np.array([orc.e4m3_decode(c) for c in range(256)])
+    kb = bf16_bits((lut[kc] * k_scale).astype(np.float32))
+    vb = bf16_bits((lut[vc] * v_scale).astype(np.float32))
+    q = normal_bf16(rng, (len(ctx), Hq, d))
+    cl = np.array(ctx, np.int32)
+    got = orc.paged_attention_fp8(q, kc, vc, k_scale, v_scale, tables, cl, 0.25)
+    ref = orc.paged_attention(q, kb, vb, tables, cl, 0.25)
+    assert np.all(np.isfinite(got))
+    assert np.array_equal(got, ref), np.abs(got - ref).max()
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
