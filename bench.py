@@ -47,7 +47,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--config", default="gqa_decode",
-                   choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen", "cb_trace"])
+                   choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen", "cb_trace",
+                            "gqa_decode_fp8"])
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -58,6 +59,10 @@ WORKLOADS = {
     "gqa_decode": ("gqa_decode_128seq_llama70b_layer", 2001,
                    {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
                     "block_size": 16, "context_lens": "uniform[500,2500]", "pool_headroom": 0.1}),
+    "gqa_decode_fp8": ("gqa_decode_128seq_llama70b_layer_fp8_e4m3_kv", 2001,
+                       {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
+                        "block_size": 16, "context_lens": "uniform[500,2500]", "pool_headroom": 0.1,
+                        "kv_dtype": "fp8_e4m3", "k_scale": 2.0 ** -6, "v_scale": 2.0 ** -6}),
     "tiny_decode": ("tiny_decode_4seq", 1001,
                     {"num_seqs": 4, "num_heads": 4, "num_kv_heads": 4, "head_dim": 64,
                      "block_size": 16, "context_lens": "uniform[1,100]", "num_blocks": 64}),
@@ -73,8 +78,14 @@ WORKLOADS = {
 
 def make_batch(config, seed):
     from pagedattention_paged_kv_gb300 import workloads as W
+    if config == "gqa_decode_fp8":
+        return W.to_fp8_pool(W.gqa_decode(seed=seed))
     return {"gqa_decode": W.gqa_decode, "tiny_decode": W.tiny_decode,
             "skewed_decode": W.skewed_decode, "mixed_varlen": W.mixed_varlen}[config](seed=seed)
+
+
+def is_fp8(b):
+    return b.meta.get("kv_dtype") == "fp8_e4m3"
 
 
 def measured_peaks():
@@ -87,7 +98,8 @@ def measured_peaks():
 
 
 def kv_bytes(b):
-    return int(b.context_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+    elem = 1 if is_fp8(b) else 2
+    return int(b.context_lens.astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * elem * 2
 
 
 def algorithmic_bytes(b):
@@ -98,7 +110,8 @@ def algorithmic_bytes(b):
     attn = kv_bytes(b) + 2 * b.q.size * 2 + nblk * 4 + b.num_seqs * 4
     if b.query_start_loc is not None:
         attn += (b.num_seqs + 1) * 4
-    new = 2 * 2 * b.k_new.size * 2 + b.k_new.shape[0] * 8
+    elem = 1 if is_fp8(b) else 2
+    new = 2 * b.k_new.size * 2 + 2 * b.k_new.size * elem + b.k_new.shape[0] * 8  # read bf16, write cache
     return attn + new, attn
 
 
@@ -181,7 +194,7 @@ def kernel_source_sha(files):
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "pkv_common.cuh",
+DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "fp8_block.cuh", "pkv_common.cuh",
                   "pkv_split.cuh", "merge.cuh")
 
 
@@ -239,9 +252,14 @@ def oracle_step_time(b, seqs):
     kc, vc = b.k_cache.copy(), b.v_cache.copy()
     t0 = time.perf_counter()
     slots = orc.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
-    orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
-    orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale,
-                        query_start_loc=b.query_start_loc, causal=b.causal, row_mask=mask)
+    if is_fp8(b):
+        ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+        orc.reshape_and_cache_fp8(kc, vc, b.k_new, b.v_new, slots, ks, vs)
+        orc.paged_attention_fp8(b.q, kc, vc, ks, vs, b.block_tables, b.context_lens, b.scale, row_mask=mask)
+    else:
+        orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
+        orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale,
+                            query_start_loc=b.query_start_loc, causal=b.causal, row_mask=mask)
     return time.perf_counter() - t0, share, orc.num_threads()
 
 
@@ -397,8 +415,14 @@ def main():
     slots = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
 
     # KV pool: resident state of the serving engine.
-    kc = torch.from_numpy(b.k_cache.view(np.int16)).to(dev).view(torch.bfloat16)
-    vc = torch.from_numpy(b.v_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    fp8 = is_fp8(b)
+    if fp8:
+        kc = torch.from_numpy(b.k_cache).to(dev)
+        vc = torch.from_numpy(b.v_cache).to(dev)
+        ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+    else:
+        kc = torch.from_numpy(b.k_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+        vc = torch.from_numpy(b.v_cache.view(np.int16)).to(dev).view(torch.bfloat16)
     arrays = {"q": b.q, "k": b.k_new, "v": b.v_new, "slots": slots, "tables": b.block_tables,
               "ctx": b.context_lens}
     if varlen:
@@ -421,13 +445,21 @@ def main():
         if varlen:
             pkv.paged_attention_varlen(o, qq, qs, kc, vc, tables, lens, b.scale, causal=b.causal,
                                        max_q_len=max_q_len, workspace=ws)
+        elif fp8:
+            pkv.paged_attention_decode_fp8(o, qq, kc, vc, tables, lens, b.scale, ks, vs, workspace=ws)
         else:
             pkv.paged_attention_decode(o, qq, kc, vc, tables, lens, b.scale, workspace=ws)
+
+    def kv_write():
+        if fp8:
+            pkv.reshape_and_cache_fp8(kc, vc, k_new, v_new, sm, ks, vs)
+        else:
+            pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
+        kv_write()
         if ev is not None:
             ev[1].record(stream)
         attention()
@@ -466,7 +498,7 @@ def main():
         def e2e_step():
             h_slots[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
             io.dev.copy_(io.host, non_blocking=True)
-            pkv.reshape_and_cache(kc, vc, k_new, v_new, sm)
+            kv_write()
             attention()
             hout.copy_(out, non_blocking=True)
             stream.synchronize()
@@ -498,7 +530,9 @@ def main():
         "metric": METRIC if args.config == "gqa_decode" else f"{name}: HBM GB/s of the step",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block permutation)",
+        "dtype": "fp8_e4m3 kv / f16 mma / f32 acc" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, random block permutation" +
+                ("; pool = e4m3 codes of x / scale)" if fp8 else ")"),
         "config": {"workload": name, **cfg, "seed": seed,
                    "sum_context": int(b.context_lens.astype(np.int64).sum()), "num_blocks": b.num_blocks,
                    "parallelism": f"replicas x{world}",
@@ -515,7 +549,7 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if not varlen:
-        traffic = recorded_traffic("decode", DECODE_SOURCES, args.config)
+        traffic = recorded_traffic("decode_fp8" if fp8 else "decode", DECODE_SOURCES, args.config)
         achieved = attn_bytes / (t_attn * 1e-3) / 1e9
         line["roofline"] = {
             "bound": "hbm", "kernel": "paged_decode_kernel (+ merge_parts_kernel, timed together)",

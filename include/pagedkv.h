@@ -75,6 +75,10 @@ extern "C" {
 
 /* ---- dtypes --------------------------------------------------------------- */
 #define PKV_DTYPE_BF16 0
+/* An FP8 cache: one OCP e4m3 code byte per element (the pages' headline model,
+ * Llama 3.3 70B, is served in FP8: [LESSON] "Numbers you should remember").  Used
+ * through the *_fp8 calls below, which take the per-tensor scales. */
+#define PKV_DTYPE_FP8_E4M3 1
 
 /* ---- ops for pkv_workspace_size ------------------------------------------- */
 #define PKV_OP_DECODE 0
@@ -115,6 +119,44 @@ int pkv_paged_attention_decode(void *out, const void *q, const void *k_cache, co
                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                float scale, int dtype, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * FP8 KV cache (e4m3 codes, one scale for K and one for V).  The pages state the
+ * cache layout and name FP8 serving but not the element encoding; the reading
+ * here: a cached code c means e4m3_value(c) * scale, where e4m3 is the OCP 8-bit
+ * floating-point format E4M3 (bias 7, 3 mantissa bits, subnormals, largest finite
+ * 448, NaN = S.1111.111, no infinities).
+ *
+ * pkv_reshape_and_cache_fp8: the same placement as pkv_reshape_and_cache; k and v
+ * are bf16 rows, k_cache and v_cache uint8 [num_blocks, block_size, num_kv_heads,
+ * head_dim].  Element x of a K row is stored as the e4m3 code nearest to
+ * fp32(x) / k_scale (one correctly rounded fp32 division), ties to the even code,
+ * magnitudes beyond 448 stored as +-448; likewise v with v_scale.  Bit-exact.
+ * Scales must be finite and > 0 (else PKV_ERR_INVALID_ARG).
+ * Supported: num_kv_heads * head_dim a multiple of 16.
+ */
+int pkv_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
+                              const int64_t *slot_mapping, int64_t num_tokens,
+                              int64_t num_blocks, int block_size, int num_kv_heads,
+                              int head_dim, float k_scale, float v_scale, void *stream);
+
+/*
+ * pkv_paged_attention_decode_fp8: pkv_paged_attention_decode over an FP8 cache,
+ * with every cached K element read as e4m3_value * k_scale and every V element as
+ * e4m3_value * v_scale.  q and out stay bf16.  On the tensor cores the products
+ * run in fp16 with fp32 accumulation: the e4m3 codes widen to fp16 exactly, q is
+ * rounded to fp16 (exact for bf16 values of magnitude in [2^-14, 65504]), the
+ * softmax weights are rounded to fp16.  Workspace as for the bf16 call
+ * (pkv_workspace_size(PKV_OP_DECODE, ...)).
+ * Supported: block_size 16, head_dim 128, the bf16 call's head counts.
+ */
+int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs,
+                                   int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks, float scale,
+                                   float k_scale, float v_scale, void *workspace,
+                                   size_t workspace_bytes, void *stream);
 
 /*
  * Varlen attention over a ragged batch in one call ([LESSON] "Chunked prefill

@@ -25,6 +25,7 @@ BLOCK_SIZE = 16
 OP_DECODE = 0
 OP_VARLEN = 1
 DTYPE_BF16 = 0
+DTYPE_FP8_E4M3 = 1
 
 _STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
            -3: "workspace too small", -4: "CUDA error", -5: "out of blocks",
@@ -62,6 +63,9 @@ def lib() -> ctypes.CDLL:
                                                  i32, i64, f32, i32, vp, sz, vp]
         L.pkv_paged_attention_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                  i32, i32, i32, i32, i64, f32, i32, i32, vp, sz, vp]
+        L.pkv_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, f32, f32, vp]
+        L.pkv_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                     i32, i64, f32, f32, f32, vp, sz, vp]
         L.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.pkv_workspace_size.restype = sz
         L.pkv_status_string.argtypes = [i32]
@@ -75,7 +79,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_block_manager_free.argtypes = [vp, vp, i64]
         L.pkv_block_manager_num_free.argtypes = [vp]
         L.pkv_block_manager_num_free.restype = i64
-        for name in ("pkv_reshape_and_cache", "pkv_paged_attention_decode",
+        for name in ("pkv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_reshape_and_cache_fp8",
+                     "pkv_paged_attention_decode_fp8",
                      "pkv_paged_attention_varlen", "pkv_get_device_error", "pkv_slot_mapping",
                      "pkv_block_manager_allocate", "pkv_block_manager_free"):
             getattr(L, name).restype = i32
@@ -172,6 +177,51 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         S, block_tables.shape[1], Hq, Hkv, d, bs, NB, float(scale), DTYPE_BF16, _ptr(ws),
         ws.numel() * ws.element_size(), _stream_ptr(stream)), "paged_attention_decode")
+
+
+def reshape_and_cache_fp8(k_cache, v_cache, k, v, slot_mapping, k_scale: float, v_scale: float,
+                          stream=None) -> None:
+    """FP8 cache: k_cache/v_cache [NB, bs, Hkv, d] uint8 (e4m3 codes) <- k/v [T, Hkv, d] bf16,
+    each element stored as e4m3(fp32(x) / scale) (k_scale for K, v_scale for V)."""
+    import torch
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, torch.uint8, n, 4)
+    for t, n in ((k, "k"), (v, "v")):
+        _require(t, torch.bfloat16, n, 3)
+    _require(slot_mapping, torch.int64, "slot_mapping", 1)
+    NB, bs, Hkv, d = k_cache.shape
+    T = k.shape[0]
+    if v_cache.shape != k_cache.shape or v.shape != k.shape or tuple(k.shape[1:]) != (Hkv, d) \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("shape mismatch")
+    _check(lib().pkv_reshape_and_cache_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v),
+                                           _ptr(slot_mapping), T, NB, bs, Hkv, d, float(k_scale),
+                                           float(v_scale), _stream_ptr(stream)), "reshape_and_cache_fp8")
+
+
+def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                               k_scale: float, v_scale: float, workspace=None, stream=None) -> None:
+    """Decode over an FP8 cache: out/q [S, Hq, d] bf16; k_cache/v_cache [NB, bs, Hkv, d] uint8
+    e4m3 codes (element = code value x k_scale / v_scale); block_tables [S, MB] int32;
+    context_lens [S] int32."""
+    import torch
+    _require(out, torch.bfloat16, "out", 3)
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.uint8, "k_cache", 4)
+    _require(v_cache, torch.uint8, "v_cache", 4)
+    _require(block_tables, torch.int32, "block_tables", 2)
+    _require(context_lens, torch.int32, "context_lens", 1)
+    S, Hq, d = q.shape
+    NB, bs, Hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("shape mismatch")
+    nbytes = workspace_size(OP_DECODE, S, S, Hq, Hkv, d, bs)
+    ws = _workspace(workspace, nbytes, q.device)
+    _check(lib().pkv_paged_attention_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        S, block_tables.shape[1], Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)), "paged_attention_decode_fp8")
 
 
 def paged_attention_varlen(out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens,

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -16,6 +17,10 @@ cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k
                                      const int64_t *slot_mapping, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int num_sms, int *err,
                                      cudaStream_t stream);
+cudaError_t launch_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
+                                         const int64_t *slot_mapping, int64_t num_tokens,
+                                         int64_t num_slots, int row_elems, float k_scale,
+                                         float v_scale, int num_sms, int *err, cudaStream_t stream);
 }
 
 // The device error word (one per device that loads the library).
@@ -83,15 +88,20 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // contiguous, so the 128-byte swizzle spreads an 8-token ldmatrix over all banks.  One
 // box moves box_heads * 2 KiB; a block's K (or V) for box_heads heads takes
 // head_dim / 64 boxes.
+// With an FP8 cache (fp8 = true) an element is one byte, so a 128-byte chunk holds 128
+// columns: head_dim 128 is one chunk and one box per block row.
 int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int block_size,
-                     int num_kv_heads, int head_dim, int box_heads) {
-    const cuuint64_t row = (cuuint64_t)num_kv_heads * head_dim * 2;  // bytes per token
-    cuuint64_t dims[5] = {64, (cuuint64_t)block_size, (cuuint64_t)num_kv_heads,
-                          (cuuint64_t)(head_dim / 64), (cuuint64_t)num_blocks};
-    cuuint64_t strides[4] = {row, (cuuint64_t)head_dim * 2, 128, row * block_size};
-    cuuint32_t box[5] = {64, (cuuint32_t)block_size, (cuuint32_t)box_heads, 1, 1};
+                     int num_kv_heads, int head_dim, int box_heads, bool fp8 = false) {
+    const int elem = fp8 ? 1 : 2;
+    const int cw = 128 / elem;  // columns per 128-byte chunk
+    const cuuint64_t row = (cuuint64_t)num_kv_heads * head_dim * elem;  // bytes per token
+    cuuint64_t dims[5] = {(cuuint64_t)cw, (cuuint64_t)block_size, (cuuint64_t)num_kv_heads,
+                          (cuuint64_t)(head_dim / cw), (cuuint64_t)num_blocks};
+    cuuint64_t strides[4] = {row, (cuuint64_t)head_dim * elem, 128, row * block_size};
+    cuuint32_t box[5] = {(cuuint32_t)cw, (cuuint32_t)block_size, (cuuint32_t)box_heads, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
+    CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                          const_cast<void *>(cache), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -124,7 +134,7 @@ struct DecodePlan {
 };
 
 int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, const DeviceInfo &d,
-                DecodePlan *p) {
+                DecodePlan *p, int elem_bytes = 2) {
     p->group = num_heads / num_kv_heads;
     p->warps_per_head = (p->group + 15) / 16;
     if (p->warps_per_head > 8) return PKV_ERR_UNSUPPORTED;
@@ -135,11 +145,14 @@ int plan_decode(int num_seqs, int num_heads, int num_kv_heads, int head_dim, con
     p->head_tiles = num_kv_heads / ht;
     p->items = num_seqs * p->head_tiles;
     if (p->items > kMaxDecodeItems) return PKV_ERR_UNSUPPORTED;
-    p->stage_bytes = ht * head_dim * kBlockSize * 2;
+    p->stage_bytes = ht * head_dim * kBlockSize * elem_bytes;
     const size_t fixed = pkv::decode_smem_bytes(0, 0, p->items);
     const int budget = d.smem_optin;
     int nst = (int)((budget - (int64_t)fixed) / (p->stage_bytes + 16));
-    if (nst > 6) nst = 6;  // deeper rings measured no faster; the rest is left free
+    // 6 bf16 stages (192 KiB in flight): deeper rings measured no faster; an FP8 ring
+    // keeps the same bytes in flight with twice the stages
+    const int cap = elem_bytes == 1 ? 12 : 6;
+    if (nst > cap) nst = cap;
     if (nst < 2) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
     p->smem = pkv::decode_smem_bytes(p->stage_bytes, nst, p->items);
@@ -173,15 +186,16 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
                const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
                int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
                int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
-               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream) {
+               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, bool fp8 = false,
+               float k_scale = 1.f, float v_scale = 1.f) {
     if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
     CUtensorMap kmap, vmap;
     int st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
-                              p.heads_per_cta);
+                              p.heads_per_cta, fp8);
     if (st == PKV_OK)
         st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
-                              p.heads_per_cta);
+                              p.heads_per_cta, fp8);
     if (st != PKV_OK) return st;
     pkv::DecodeArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -201,12 +215,13 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     a.grid = p.grid;
     a.min_blocks_per_cta = 8;
     a.num_blocks = num_blocks;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale_log2 = scale * 1.4426950408889634f * k_scale;
+    a.v_scale = v_scale;
     a.ws_jobs = reinterpret_cast<pkv::MergeJob *>(ws + p.off_jobs);
     a.ws_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
     a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
     a.err = d.err;
-    return pkv::launch_paged_decode(head_dim, kmap, vmap, a, p.smem, stream) == cudaSuccess
+    return pkv::launch_paged_decode(head_dim, fp8, kmap, vmap, a, p.smem, stream) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
 }
@@ -263,6 +278,31 @@ extern "C" int pkv_reshape_and_cache(void *k_cache, void *v_cache, const void *k
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+extern "C" int pkv_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
+                                         const int64_t *slot_mapping, int64_t num_tokens,
+                                         int64_t num_blocks, int block_size, int num_kv_heads,
+                                         int head_dim, float k_scale, float v_scale, void *stream) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    const int64_t row_elems = (int64_t)num_kv_heads * head_dim;
+    if (row_elems % 16 != 0 || row_elems > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    int st = device_info(&d);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_reshape_and_cache_fp8(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                                                      num_blocks * block_size, (int)row_elems, k_scale,
+                                                      v_scale, d->sms, d->err,
+                                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 extern "C" size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,
                                      int num_kv_heads, int head_dim, int block_size) {
     if (check_common(num_seqs, 0, num_heads, num_kv_heads, head_dim, block_size, 0,
@@ -307,6 +347,37 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *q, const void *
                       max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
                       static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
                       static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_tables,
+                                              const int32_t *context_lens, int num_seqs,
+                                              int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                              int head_dim, int block_size, int64_t num_blocks,
+                                              float scale, float k_scale, float v_scale,
+                                              void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, PKV_DTYPE_BF16);
+    if (st != PKV_OK) return st;
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    st = device_info(&d);
+    if (st != PKV_OK) return st;
+    DecodePlan p;
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p, 1);
+    if (st != PKV_OK) return st;
+    return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
+                      static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
+                      static_cast<cudaStream_t>(stream), true, k_scale, v_scale);
 }
 
 extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,

@@ -25,6 +25,7 @@
 //  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
 //    reports PKV_DEVERR_TIMEOUT instead of hanging.
 #include "attn_block.cuh"
+#include "fp8_block.cuh"
 #include "merge.cuh"
 #include "paged_decode.cuh"
 #include "pkv_split.cuh"
@@ -150,20 +151,22 @@ __device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pr
     }
 }
 
-template <int D>
+// FP8: the cache holds e4m3 codes (head_dim 128 only); see fp8_block.cuh.
+template <int D, bool FP8>
 __global__ void __launch_bounds__(288, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
-    constexpr int KSTEPS = D / 16;  // k-steps of the QK^T MMA
-    constexpr int NT_D = D / 8;     // n-tiles of the PV MMA
-    constexpr int DCH = D / 64;     // 64-wide column chunks (one TMA box each)
+    static_assert(!FP8 || D == 128, "the FP8 cache path is built for head_dim 128");
+    constexpr int KSTEPS = D / 16;         // k-steps of the QK^T MMA
+    constexpr int NT_D = D / 8;            // n-tiles of the PV MMA
+    constexpr int DCH = FP8 ? 1 : D / 64;  // TMA boxes per block row (128 bytes each)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int HT = a.heads_per_cta;
     const int NST = a.num_stages;
-    const uint32_t stage_bytes = (uint32_t)HT * D * kBS * 2;
+    const uint32_t stage_bytes = (uint32_t)HT * D * kBS * (FP8 ? 1 : 2);
     const uint32_t chunk_stride = (uint32_t)HT * kBS * 128;  // between 64-column sub-tiles
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * stage_bytes);
     uint64_t *empty = full + NST;
@@ -284,7 +287,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
         // Q fragments (A operand, rows = query heads of the group).
         uint32_t qa[KSTEPS][4];
-        {
+        if constexpr (FP8) {
+            load_q_fp8order(qa, a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D, rows_valid, lane);
+        } else {
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
                 a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D);
             const bool v0 = g_row < rows_valid, v1 = g_row + 8 < rows_valid;
@@ -306,7 +311,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             // ---- S = Q K^T over the block's 16 tokens ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
             float sacc[2][4];
-            qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
+            if constexpr (FP8) qk_block_fp8(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), lane);
+            else qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
@@ -330,13 +336,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                 }
             }
             uint32_t pa[4];
-            softmax_update<D>(st, sacc, pa);
+            softmax_update<D, FP8>(st, sacc, pa);
 
             // ---- O += P V ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
             const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-            if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
-            else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
+            if constexpr (FP8) {
+                if (tail) pv_block_fp8<true>(st.o, pa, vtile, valid, lane);
+                else pv_block_fp8<false>(st.o, pa, vtile, valid, lane);
+            } else {
+                if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
+                else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
@@ -351,7 +362,55 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         finish_sums<D>(st);
         const int64_t seg_beg = max64(lo, item_beg);
         const bool whole = seg_beg == item_beg && seg_end == item_end;
-        if (whole) {
+        if constexpr (FP8) {
+            // accumulators hold dims 32t + j (columns 0, 2) and 32t + 16 + j (1, 3); the
+            // V scale comes in here
+            const float vs = a.v_scale;
+            const bool w0 = g_row < rows_valid, w1 = g_row + 8 < rows_valid;
+            if (whole) {
+                const float inv0 = vs / st.l0, inv1 = vs / st.l1;
+                __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D + 32 * q4;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        uint4 x0, x1;
+                        uint32_t *p0 = &x0.x, *p1 = &x1.x;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int j = 8 * i + 2 * k;
+                            p0[k] = pack_bf16x2(st.o[j][half] * inv0, st.o[j + 1][half] * inv0);
+                            p1[k] = pack_bf16x2(st.o[j][2 + half] * inv1, st.o[j + 1][2 + half] * inv1);
+                        }
+                        if (w0) *reinterpret_cast<uint4 *>(orow + g_row * D + 16 * half + 8 * i) = x0;
+                        if (w1) *reinterpret_cast<uint4 *>(orow + (g_row + 8) * D + 16 * half + 8 * i) = x1;
+                    }
+            } else {
+                const int slot = part_slot(c, item_beg, T, ge);
+                const int rows = HT * group;
+                const int row0 = hh * group + r0;  // row inside the item
+                float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D + 32 * q4;
+                float2 *mlb = a.ws_ml + (int64_t)slot * rows + row0;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = 4 * i;
+                        if (w0)
+                            *reinterpret_cast<float4 *>(ob + g_row * D + 16 * half + j) =
+                                make_float4(st.o[j][half] * vs, st.o[j + 1][half] * vs,
+                                            st.o[j + 2][half] * vs, st.o[j + 3][half] * vs);
+                        if (w1)
+                            *reinterpret_cast<float4 *>(ob + (g_row + 8) * D + 16 * half + j) =
+                                make_float4(st.o[j][2 + half] * vs, st.o[j + 1][2 + half] * vs,
+                                            st.o[j + 2][2 + half] * vs, st.o[j + 3][2 + half] * vs);
+                    }
+                if (q4 == 0) {
+                    if (w0) mlb[g_row] = make_float2(st.m0, st.l0);
+                    if (w1) mlb[g_row + 8] = make_float2(st.m1, st.l1);
+                }
+            }
+        } else if (whole) {
             const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
             __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
 #pragma unroll
@@ -387,10 +446,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 }
 
-template __global__ void paged_decode_kernel<64>(const __grid_constant__ CUtensorMap,
-                                                 const __grid_constant__ CUtensorMap, const DecodeArgs);
-template __global__ void paged_decode_kernel<128>(const __grid_constant__ CUtensorMap,
-                                                  const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<64, false>(const __grid_constant__ CUtensorMap,
+                                                        const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<128, false>(const __grid_constant__ CUtensorMap,
+                                                         const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<128, true>(const __grid_constant__ CUtensorMap,
+                                                        const __grid_constant__ CUtensorMap, const DecodeArgs);
 
 // ---- host-side launch ----------------------------------------------------------
 
@@ -399,14 +460,14 @@ size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items) {
            4 * (size_t)(num_items + 1);
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
                                    const DecodeArgs &a, size_t smem, cudaStream_t stream) {
     const int ncw = a.heads_per_cta * a.warps_per_head;
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(paged_decode_kernel<D>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
+    e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
                    v_map, a);
     if (e != cudaSuccess) return e;
     MergeArgs m;
@@ -419,10 +480,12 @@ static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &
     return launch_merge<D>(m, a.grid, stream);
 }
 
-cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
+cudaError_t launch_paged_decode(int head_dim, bool fp8, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                 const DecodeArgs &a, size_t smem, cudaStream_t stream) {
-    return head_dim == 128 ? launch_decode_d<128>(k_map, v_map, a, smem, stream)
-                           : launch_decode_d<64>(k_map, v_map, a, smem, stream);
+    if (fp8) return head_dim == 128 ? launch_decode_d<128, true>(k_map, v_map, a, smem, stream)
+                                    : cudaErrorInvalidValue;
+    return head_dim == 128 ? launch_decode_d<128, false>(k_map, v_map, a, smem, stream)
+                           : launch_decode_d<64, false>(k_map, v_map, a, smem, stream);
 }
 
 }  // namespace pkv

@@ -27,7 +27,8 @@ struct DecodeArgs {
     int grid;            // CTAs launched
     int min_blocks_per_cta;
     int64_t num_blocks;
-    float scale_log2;    // scale * log2(e)
+    float scale_log2;    // scale * log2(e) (times the K scale for an FP8 cache)
+    float v_scale;       // FP8 cache: V element = code value * v_scale (1 otherwise)
     MergeJob *ws_jobs;   // [grid]
     float2 *ws_ml;       // [2 * grid][heads_per_cta * group]  (running max, sum)
     float *ws_o;         // [2 * grid][heads_per_cta * group][head_dim]
@@ -35,7 +36,7 @@ struct DecodeArgs {
 };
 
 size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items);
-cudaError_t launch_paged_decode(int head_dim, const CUtensorMap &k_map, const CUtensorMap &v_map,
+cudaError_t launch_paged_decode(int head_dim, bool fp8, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                 const DecodeArgs &a, size_t smem, cudaStream_t stream);
 
 }  // namespace pkv

@@ -9,6 +9,8 @@
 // One warp per (token, K-or-V) row: the row (num_kv_heads * head_dim * 2 bytes,
 // 2 KiB for Llama-70B shapes) moves as 16-byte vectors, fully coalesced on both sides.
 // The source is read once (no L1 allocation); the destination is written normally.
+#include <cuda_fp8.h>
+
 #include "attn_block.cuh"
 #include "pkv_common.cuh"
 
@@ -37,6 +39,66 @@ reshape_and_cache_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cach
         uint4 *dst = (is_v ? v_cache : k_cache) + slot * row_vecs;
         for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldcs(src + i);
     }
+}
+
+// FP8 cache: each element of a row is stored as the e4m3 code nearest to
+// fp32(x) / scale (IEEE division, round-to-nearest-even conversion saturating at
+// +-448).  One warp per (token, K-or-V) row; a lane turns 16 bf16 (32 bytes, two
+// 16-byte loads) into 16 codes (one 16-byte store).
+__device__ __forceinline__ uint32_t e4m3_of(uint32_t bf16_bits, float scale) {
+    const float y = __fdiv_rn(__uint_as_float(bf16_bits << 16), scale);
+    return (uint32_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4_of(uint32_t w0, uint32_t w1, float scale) {
+    return e4m3_of(w0 & 0xFFFFu, scale) | (e4m3_of(w0 >> 16, scale) << 8) |
+           (e4m3_of(w1 & 0xFFFFu, scale) << 16) | (e4m3_of(w1 >> 16, scale) << 24);
+}
+
+__global__ void __launch_bounds__(256)
+reshape_and_cache_fp8_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                             const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                             const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                             int64_t num_slots, int row_groups, float k_scale, float v_scale,
+                             int *err) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         w < 2 * num_tokens; w += warps) {
+        const int64_t t = w >> 1;
+        const bool is_v = (w & 1) != 0;
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;  // padding token
+        if (slot >= num_slots) {
+            if (lane == 0 && !is_v) flag_error(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const float sc = is_v ? v_scale : k_scale;
+        const uint4 *src = (is_v ? v : k) + t * row_groups * 2;  // 16 bf16 = 2 vectors
+        uint4 *dst = (is_v ? v_cache : k_cache) + slot * row_groups;  // 16 codes = 1 vector
+        for (int i = lane; i < row_groups; i += 32) {
+            const uint4 a = __ldcs(src + 2 * i), b = __ldcs(src + 2 * i + 1);
+            dst[i] = make_uint4(e4m3x4_of(a.x, a.y, sc), e4m3x4_of(a.z, a.w, sc), e4m3x4_of(b.x, b.y, sc),
+                                e4m3x4_of(b.z, b.w, sc));
+        }
+    }
+}
+
+cudaError_t launch_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
+                                         const int64_t *slot_mapping, int64_t num_tokens,
+                                         int64_t num_slots, int row_elems, float k_scale,
+                                         float v_scale, int num_sms, int *err, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int warps_per_cta = 8;
+    int64_t ctas = (2 * num_tokens + warps_per_cta - 1) / warps_per_cta;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (ctas > cap) ctas = cap;
+    return launch_pdl(reshape_and_cache_fp8_kernel, dim3((unsigned)ctas), dim3(warps_per_cta * 32), 0,
+                      stream, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+                      num_tokens, num_slots, row_elems / 16, k_scale, v_scale, err);
 }
 
 cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,

@@ -175,6 +175,37 @@ def make_batch(name: str, *, context_lens, q_lens, num_heads: int, num_kv_heads:
 
 
 # ---------------------------------------------------------------------------
+# FP8 pool: the same step with the pool held as e4m3 codes.
+# ---------------------------------------------------------------------------
+
+# K and V scale of the FP8 workloads: a power of two, so x / scale is exact, and
+# N(0,1) values times 64 stay far inside the e4m3 range (+-448).
+FP8_SCALE = 2.0 ** -6
+
+
+def to_fp8_pool(b: PagedBatch, k_scale: float = FP8_SCALE, v_scale: float = FP8_SCALE,
+                chunk_blocks: int = 2048) -> PagedBatch:
+    """The same step with an FP8 pool: each pool byte is torch's float8_e4m3fn cast
+    (a library conversion) of the bf16 pool value divided by the scale; NaN slots
+    become the NaN code.  The new K/V rows stay bf16 (the KV write quantises them)."""
+    import dataclasses
+
+    import torch
+
+    def cast(pool, scale):
+        out = np.empty(pool.shape, dtype=np.uint8)
+        for i in range(0, pool.shape[0], chunk_blocks):
+            f = bf16_to_f32(pool[i:i + chunk_blocks]) / np.float32(scale)
+            out[i:i + chunk_blocks] = torch.from_numpy(f).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return out
+
+    return dataclasses.replace(b, name=b.name + "_fp8", k_cache=cast(b.k_cache, k_scale),
+                               v_cache=cast(b.v_cache, v_scale),
+                               meta={**b.meta, "kv_dtype": "fp8_e4m3", "k_scale": float(k_scale),
+                                     "v_scale": float(v_scale)})
+
+
+# ---------------------------------------------------------------------------
 # The five workloads.  Seeds are (workload index) * 1000 + 1.
 # ---------------------------------------------------------------------------
 

@@ -79,3 +79,40 @@ def compare(gpu: np.ndarray, ref: np.ndarray, rows=None):
                              f"max_rel {max_rel:.3g}); first {idx.tolist()} "
                              f"gpu {gpu[tuple(idx[0])]:.6g} ref {ref[tuple(idx[0])]:.6g}")
     return max_abs, max_rel
+
+
+def torch_u8(a: np.ndarray, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def gpu_step_fp8(b: PagedBatch, workspace=None):
+    """FP8 pool (b from workloads.to_fp8_pool): slot mapping, the quantising KV write
+    and decode through the library.  Returns (out fp64, k_cache codes, v_cache codes,
+    device error flags)."""
+    import torch
+    ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+    slots = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+    kc, vc = torch_u8(b.k_cache), torch_u8(b.v_cache)
+    k, v, q = torch_bf16(b.k_new), torch_bf16(b.v_new), torch_bf16(b.q)
+    sm = torch.from_numpy(slots).cuda()
+    bt = torch.from_numpy(b.block_tables).cuda()
+    cl = torch.from_numpy(b.context_lens).cuda()
+    out = torch.full_like(q, float("nan"))
+    pkv.reshape_and_cache_fp8(kc, vc, k, v, sm, ks, vs)
+    assert b.query_start_loc is None, "the FP8 path is decode only"
+    pkv.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, b.scale, ks, vs, workspace=workspace)
+    err = pkv.get_device_error()
+    return bf16_bits_to_f64(bf16_to_np(out)), kc.cpu().numpy(), vc.cpu().numpy(), err
+
+
+def oracle_step_fp8(b: PagedBatch, row_mask=None):
+    """The same FP8 step through the oracle."""
+    orc = oracle.load()
+    ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+    slots = orc.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+    kc, vc = b.k_cache.copy(), b.v_cache.copy()
+    orc.reshape_and_cache_fp8(kc, vc, b.k_new, b.v_new, slots, ks, vs)
+    out = orc.paged_attention_fp8(b.q, kc, vc, ks, vs, b.block_tables, b.context_lens, b.scale,
+                                  row_mask=row_mask)
+    return out, kc, vc
