@@ -159,6 +159,19 @@ int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * Block copy (the device half of copy-on-write, [LPNH] §4.3): for each i < num_pairs,
+ * with (src, dst) = (block_pairs[2i], block_pairs[2i+1]) (device int32),
+ *     k_cache[dst] = k_cache[src]  and  v_cache[dst] = v_cache[src]   (whole blocks)
+ * of a pool laid out as [num_blocks, block_size, num_kv_heads, head_dim] with elements
+ * of `dtype` (PKV_DTYPE_BF16 or PKV_DTYPE_FP8_E4M3).  Bit-exact.  A dst must not appear
+ * as another pair's src or dst in the same call (the copies run in parallel).  Ids outside
+ * the pool are skipped and flagged PKV_DEVERR_BLOCK_ID.
+ */
+int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pairs, int64_t num_pairs,
+                    int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
+                    void *stream);
+
+/*
  * Varlen attention over a ragged batch in one call ([LESSON] "Chunked prefill
  * protects the TTFT tail", "What the scheduler looks like": prefill chunks and
  * single-token decodes in one fused GPU call).  Sequence s owns query rows
@@ -243,10 +256,27 @@ pkv_block_manager *pkv_block_manager_create(int64_t num_blocks, int block_size);
 void pkv_block_manager_destroy(pkv_block_manager *bm);
 /* Writes n ids to host_ids_out; PKV_ERR_OOM (nothing taken) if fewer are free. */
 int pkv_block_manager_allocate(pkv_block_manager *bm, int64_t n, int32_t *host_ids_out);
-/* Returns ids to the free list; PKV_ERR_INVALID_ARG (nothing returned) if an id is
- * outside the pool or not currently allocated. */
+/* Drops one reference per listed id; a block whose last reference goes returns to the
+ * tail of the free list (in the order listed).  PKV_ERR_INVALID_ARG (nothing changed)
+ * if an id is outside the pool or listed more often than it is held. */
 int pkv_block_manager_free(pkv_block_manager *bm, const int32_t *host_ids, int64_t n);
 int64_t pkv_block_manager_num_free(const pkv_block_manager *bm);
+
+/*
+ * Shared read-only blocks ([LPNH] §4.3 prefix caching: requests with the same
+ * system-prompt prefix reuse one set of read-only KV blocks).  A block allocated once
+ * has one reference; share(ids) adds one reference per listed id (each must be held);
+ * free drops one.  ref_count(id) returns the count (PKV_ERR_INVALID_ARG outside the
+ * pool).  copy_on_write(id): the caller holds id and is about to write into it; if it is
+ * the only holder, *host_new_id = id and 0 is returned (write in place); otherwise a
+ * fresh block is taken from the free list, the caller's reference moves to it,
+ * *host_new_id = the new id and 1 is returned -- the caller must then copy the block
+ * on the device (pkv_copy_blocks) before writing.  PKV_ERR_OOM (nothing changed) if a
+ * copy is needed and no block is free.
+ */
+int pkv_block_manager_share(pkv_block_manager *bm, const int32_t *host_ids, int64_t n);
+int pkv_block_manager_ref_count(const pkv_block_manager *bm, int32_t id);
+int pkv_block_manager_copy_on_write(pkv_block_manager *bm, int32_t id, int32_t *host_new_id);
 
 #ifdef __cplusplus
 }

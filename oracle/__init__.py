@@ -58,6 +58,8 @@ class Oracle:
         lib.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                i32, i64, dbl, i32, vp]
         lib.oracle_paged_attention.restype = i32
+        lib.oracle_copy_blocks.argtypes = [vp, vp, vp, i64, i64, i64]
+        lib.oracle_copy_blocks.restype = i32
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_decode.restype = dbl
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
@@ -124,6 +126,18 @@ class Oracle:
             raise ValueError("oracle_paged_attention: invalid input")
         return out
 
+
+    # -- copy-on-write block copy -----------------------------------------------
+    def copy_blocks(self, k_cache, v_cache, pairs) -> None:
+        """Copies whole blocks in place (any dtype; pairs int32 [n, 2] of (src, dst))."""
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        assert k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype
+        pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+        NB = k_cache.shape[0]
+        block_bytes = k_cache.nbytes // NB if NB else 0
+        rc = self.lib.oracle_copy_blocks(_p(k_cache), _p(v_cache), _p(pr), pr.shape[0], NB, block_bytes)
+        if rc != 0:
+            raise ValueError("oracle_copy_blocks: block id outside the pool")
 
     # -- FP8 (OCP e4m3) cache ---------------------------------------------------
     def e4m3_decode(self, code: int) -> float:

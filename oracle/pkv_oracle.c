@@ -219,6 +219,30 @@ int oracle_reshape_and_cache_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint1
     return status;
 }
 
+/*
+ * Block copy (copy-on-write, [LPNH] §4.3 shared read-only prefix blocks): for each pair
+ * (src, dst), every byte of block dst of both caches becomes the byte of block src.
+ * Pairs are applied in order.  -1 (having applied the valid pairs) if an id is outside
+ * the pool.
+ */
+int oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pairs, int64_t num_pairs,
+                       int64_t num_blocks, int64_t block_bytes)
+{
+    int status = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            status = -1;
+            continue;
+        }
+        for (int64_t b = 0; b < block_bytes; ++b) {
+            k_cache[dst * block_bytes + b] = k_cache[src * block_bytes + b];
+            v_cache[dst * block_bytes + b] = v_cache[src * block_bytes + b];
+        }
+    }
+    return status;
+}
+
 /* Check the inputs that decide which memory the attention reads. */
 static int check_sequence(const int32_t *block_tables, int64_t max_blocks_per_seq,
                           int64_t num_blocks, int block_size, int64_t s, int64_t ctx,

@@ -40,6 +40,10 @@ int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cac
                            int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                            double scale, int causal, const uint8_t *row_mask);
 
+/* Block copy: block dst of both caches (block_bytes bytes each) becomes block src. */
+int oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *pairs, int64_t num_pairs,
+                       int64_t num_blocks, int64_t block_bytes);
+
 /* FP8 (OCP e4m3) cache: k_cache, v_cache hold one code byte per element.  The codec
  * functions are exported for the tests. */
 double oracle_e4m3_decode(uint8_t code);

@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.pkv_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, f32, f32, vp]
         L.pkv_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      i32, i64, f32, f32, f32, vp, sz, vp]
+        L.pkv_copy_blocks.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        L.pkv_block_manager_share.argtypes = [vp, vp, i64]
+        L.pkv_block_manager_ref_count.argtypes = [vp, ctypes.c_int32]
+        L.pkv_block_manager_copy_on_write.argtypes = [vp, ctypes.c_int32, vp]
         L.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.pkv_workspace_size.restype = sz
         L.pkv_status_string.argtypes = [i32]
@@ -82,7 +86,9 @@ def lib() -> ctypes.CDLL:
         for name in ("pkv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_reshape_and_cache_fp8",
                      "pkv_paged_attention_decode_fp8",
                      "pkv_paged_attention_varlen", "pkv_get_device_error", "pkv_slot_mapping",
-                     "pkv_block_manager_allocate", "pkv_block_manager_free"):
+                     "pkv_block_manager_allocate", "pkv_block_manager_free", "pkv_copy_blocks",
+                     "pkv_block_manager_share", "pkv_block_manager_ref_count",
+                     "pkv_block_manager_copy_on_write"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -254,6 +260,26 @@ def paged_attention_varlen(out, q, query_start_loc, k_cache, v_cache, block_tabl
         ws.numel() * ws.element_size(), _stream_ptr(stream)), "paged_attention_varlen")
 
 
+def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """k_cache[dst] = k_cache[src], v_cache[dst] = v_cache[src] for each row (src, dst) of
+    block_pairs (int32 [n, 2] on the device); caches bf16 or uint8 (FP8 codes)."""
+    import torch
+    if k_cache.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif k_cache.dtype == torch.uint8:
+        dt = DTYPE_FP8_E4M3
+    else:
+        raise ValueError("k_cache must be bf16 or uint8")
+    _require(k_cache, k_cache.dtype, "k_cache", 4)
+    _require(v_cache, k_cache.dtype, "v_cache", 4)
+    _require(block_pairs, torch.int32, "block_pairs", 2)
+    if v_cache.shape != k_cache.shape or block_pairs.shape[1] != 2:
+        raise ValueError("shape mismatch")
+    NB, bs, Hkv, d = k_cache.shape
+    _check(lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], NB,
+                                 bs, Hkv, d, dt, _stream_ptr(stream)), "copy_blocks")
+
+
 def get_device_error(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the device error flags."""
     r = lib().pkv_get_device_error(_stream_ptr(stream))
@@ -312,3 +338,24 @@ class BlockManager:
 
     def num_free(self) -> int:
         return int(lib().pkv_block_manager_num_free(self._h))
+
+    def share(self, ids) -> None:
+        """One more holder for each listed (held) block: read-only sharing."""
+        arr = np.ascontiguousarray(list(ids), dtype=np.int32)
+        _check(lib().pkv_block_manager_share(self._h, arr.ctypes.data, arr.shape[0]), "share")
+
+    def ref_count(self, block_id: int) -> int:
+        r = int(lib().pkv_block_manager_ref_count(self._h, int(block_id)))
+        if r < 0:
+            raise PagedKVError(r, "ref_count")
+        return r
+
+    def copy_on_write(self, block_id: int) -> tuple[int, bool]:
+        """(id to write into, whether the block must be copied there first)."""
+        new = ctypes.c_int32(-1)
+        st = int(lib().pkv_block_manager_copy_on_write(self._h, int(block_id), ctypes.byref(new)))
+        if st == -5:
+            raise OutOfBlocks(st, "copy_on_write")
+        if st < 0:
+            raise PagedKVError(st, "copy_on_write")
+        return int(new.value), st == 1

@@ -17,6 +17,9 @@ cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k
                                      const int64_t *slot_mapping, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int num_sms, int *err,
                                      cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int64_t num_pairs,
+                               int64_t num_blocks, int64_t block_bytes, int num_sms, int *err,
+                               cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
                                          const int64_t *slot_mapping, int64_t num_tokens,
                                          int64_t num_slots, int row_elems, float k_scale,
@@ -300,6 +303,27 @@ extern "C" int pkv_reshape_and_cache_fp8(void *k_cache, void *v_cache, const voi
                                                       num_blocks * block_size, (int)row_elems, k_scale,
                                                       v_scale, d->sms, d->err,
                                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pairs,
+                               int64_t num_pairs, int64_t num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, int dtype, void *stream) {
+    if (num_pairs < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_BF16 && dtype != PKV_DTYPE_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_INVALID_ARG;
+    const int64_t block_bytes =
+        (int64_t)block_size * num_kv_heads * head_dim * (dtype == PKV_DTYPE_BF16 ? 2 : 1);
+    if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4))
+        return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    int st = device_info(&d);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, num_blocks, block_bytes,
+                                            d->sms, d->err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

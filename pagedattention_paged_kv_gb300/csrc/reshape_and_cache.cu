@@ -101,6 +101,40 @@ cudaError_t launch_reshape_and_cache_fp8(void *k_cache, void *v_cache, const voi
                       num_tokens, num_slots, row_elems / 16, k_scale, v_scale, err);
 }
 
+// Copy-on-write support: for each (src, dst) pair, block dst of both caches becomes a
+// copy of block src.  One CTA per pair (grid-stride), 16-byte vectors.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int32_t *__restrict__ pairs, int64_t num_pairs, int64_t num_blocks,
+                   int64_t block_vecs, int *err) {
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t p = blockIdx.x; p < num_pairs; p += gridDim.x) {
+        const int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (threadIdx.x == 0) flag_error(err, PKV_DEVERR_BLOCK_ID);
+            continue;
+        }
+        const uint4 *ks = k_cache + src * block_vecs, *vs = v_cache + src * block_vecs;
+        uint4 *kd = k_cache + dst * block_vecs, *vd = v_cache + dst * block_vecs;
+        for (int64_t i = threadIdx.x; i < block_vecs; i += blockDim.x) {
+            kd[i] = ks[i];
+            vd[i] = vs[i];
+        }
+    }
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int64_t num_pairs,
+                               int64_t num_blocks, int64_t block_bytes, int num_sms, int *err,
+                               cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    int64_t ctas = num_pairs;
+    if (ctas > (int64_t)num_sms * 4) ctas = (int64_t)num_sms * 4;
+    return launch_pdl(copy_blocks_kernel, dim3((unsigned)ctas), dim3(256), 0, stream,
+                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, num_pairs,
+                      num_blocks, block_bytes / 16, err);
+}
+
 cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
                                      const int64_t *slot_mapping, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int num_sms, int *err,

@@ -24,6 +24,8 @@ keep their admission order in the batch.
 """
 from __future__ import annotations
 
+import hashlib
+from collections import OrderedDict
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -42,6 +44,8 @@ class Sequence:
     computed: int = 0         # tokens whose K/V are in the cache
     decoded: int = 0          # output tokens produced
     preemptions: int = 0
+    prompt_tokens: np.ndarray | None = None  # token ids (needed for prefix caching only)
+    cached_tokens: int = 0    # prompt tokens whose K/V came from the prefix cache
 
     def __post_init__(self):
         if self.prefill_target == 0:
@@ -79,6 +83,7 @@ class IterationBatch:
     admitted: int = 0
     finished: int = 0
     preempted: int = 0
+    copies: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int32))  # (src, dst) block copies to run first
 
     @property
     def num_seqs(self) -> int:
@@ -93,10 +98,77 @@ class IterationBatch:
         return max((it.q_len for it in self.items), default=0)
 
 
+class PrefixCache:
+    """Read-only reuse of a shared prompt prefix's KV blocks ("vLLM推理引擎架构PagedAttention
+    机制与高吞吐推理" (lpnh.cn) §4.3: requests with the same system-prompt prefix reuse one
+    set of read-only blocks, at the cost of prefix matching in the scheduler).
+
+    Only full blocks are cached.  The key of prompt block i is a SHA-256 chain over the
+    token ids of blocks 0..i, so equal keys mean equal prefixes (up to a hash collision).
+    The cache holds one reference on every block it lists; blocks that only the cache still
+    holds are evicted, least recently matched first, when the pool runs short.
+    """
+
+    def __init__(self, block_manager: BlockManager, block_size: int = BLOCK_SIZE):
+        self.bm = block_manager
+        self.block_size = int(block_size)
+        self.blocks: OrderedDict[bytes, int] = OrderedDict()
+        self.hits = 0      # blocks reused
+        self.inserted = 0
+        self.evicted = 0
+
+    def _keys(self, tokens, n_blocks):
+        h = b""
+        bs = self.block_size
+        for i in range(n_blocks):
+            blk = np.ascontiguousarray(tokens[i * bs:(i + 1) * bs], dtype=np.int64).tobytes()
+            h = hashlib.sha256(h + blk).digest()
+            yield h
+
+    def match(self, tokens, max_blocks: int) -> list:
+        """Ids of the longest cached run of the prompt's first full blocks (<= max_blocks)."""
+        ids = []
+        for key in self._keys(tokens, max_blocks):
+            b = self.blocks.get(key)
+            if b is None:
+                break
+            self.blocks.move_to_end(key)
+            ids.append(b)
+        self.hits += len(ids)
+        return ids
+
+    def insert(self, tokens, block_table, n_full: int) -> None:
+        """Lists the sequence's first n_full blocks (their K/V is computed); the cache takes
+        a reference on each block it did not list yet."""
+        for i, key in enumerate(self._keys(tokens, n_full)):
+            if key not in self.blocks:
+                b = block_table[i]
+                self.bm.share([b])
+                self.blocks[key] = b
+                self.inserted += 1
+
+    def evict(self, n: int) -> int:
+        """Frees up to n blocks that only the cache holds; returns how many."""
+        freed = 0
+        for key in list(self.blocks):
+            if freed >= n:
+                break
+            b = self.blocks[key]
+            if self.bm.ref_count(b) == 1:
+                del self.blocks[key]
+                self.bm.free([b])
+                freed += 1
+        self.evicted += freed
+        return freed
+
+
 class Scheduler:
     def __init__(self, block_manager: BlockManager, max_num_seqs: int = 128, chunk_size: int = 512,
-                 block_size: int = BLOCK_SIZE, max_num_batched_tokens: int | None = None):
+                 block_size: int = BLOCK_SIZE, max_num_batched_tokens: int | None = None,
+                 prefix_cache: bool = False):
         self.bm = block_manager
+        self.cache = PrefixCache(block_manager, block_size) if prefix_cache else None
+        self._copies: list = []
         self.max_num_seqs = int(max_num_seqs)
         self.chunk_size = int(chunk_size)
         self.block_size = int(block_size)
@@ -114,12 +186,48 @@ class Scheduler:
     def _blocks_for(self, tokens: int) -> int:
         return -(-tokens // self.block_size)
 
+    def _allocate(self, n: int) -> list:
+        """n fresh blocks, evicting cache-only blocks first if the pool is short."""
+        if self.cache is not None and self.bm.num_free() < n:
+            self.cache.evict(n - self.bm.num_free())
+        return self.bm.allocate(n)
+
+    def fork(self, parent: Sequence, seq_id: int, output_len: int) -> Sequence:
+        """A new sequence that continues from parent's current state (e.g. another sample
+        of the same prompt): it shares all of parent's blocks read-only; whichever of them
+        first writes into a shared block gets a private copy (copy-on-write)."""
+        child = Sequence(seq_id, parent.prompt_len, output_len, parent.arrival, list(parent.block_table),
+                         parent.prefill_target, parent.computed, parent.decoded, 0, parent.prompt_tokens)
+        self.bm.share(child.block_table)
+        self.running.append(child)
+        return child
+
+    def _own_block(self, s: Sequence, pos: int) -> bool:
+        """Makes the block holding position pos private to s before it is written."""
+        i = pos // self.block_size
+        if i >= len(s.block_table):
+            return True
+        b = s.block_table[i]
+        if self.bm.ref_count(b) == 1:
+            return True
+        if self.cache is not None and self.bm.num_free() == 0:
+            self.cache.evict(1)
+        try:
+            new, copied = self.bm.copy_on_write(b)
+        except OutOfBlocks:
+            return False
+        if copied:
+            self._copies.append((b, new))
+            s.block_table[i] = new
+        return True
+
     def _preempt(self, seq: Sequence) -> None:
         """Free everything the sequence holds; it recomputes its tokens later."""
         self.bm.free(seq.block_table)
         seq.block_table = []
         seq.prefill_target = seq.prompt_len + seq.decoded
         seq.computed = 0
+        seq.cached_tokens = 0
         seq.preemptions += 1
         self.total_preemptions += 1
         self.waiting.append(seq)
@@ -138,28 +246,43 @@ class Scheduler:
             else:
                 keep.append(s)
         self.running = keep
-        # (2) growth: a decode step writing position p needs block p // block_size
+        # (2) growth: a decode step writing position p needs block p // block_size (and
+        # needs it to itself: copy-on-write of a block shared by a fork)
         keep = []
         for s in self.running:
             if not s.in_prefill:
                 pos = s.computed
                 need = self._blocks_for(pos + 1) - len(s.block_table)
-                if need > 0:
-                    try:
-                        s.block_table.extend(self.bm.allocate(need))
-                    except OutOfBlocks:
-                        self._preempt(s)
-                        preempted += 1
-                        continue
+                try:
+                    if need > 0:
+                        s.block_table.extend(self._allocate(need))
+                    elif not self._own_block(s, pos):
+                        raise OutOfBlocks(-5, "copy_on_write")
+                except OutOfBlocks:
+                    self._preempt(s)
+                    preempted += 1
+                    continue
             keep.append(s)
         self.running = keep
-        # (3) admission from the head of the waiting queue
+        # (3) admission from the head of the waiting queue; with the prefix cache, the
+        # longest cached run of the prompt's full blocks is shared instead of recomputed
+        # (never the block of the prompt's last token, which must be computed)
         while self.waiting and len(self.running) < self.max_num_seqs:
             s = self.waiting[0]
+            hit = []
+            if self.cache is not None and s.prompt_tokens is not None:
+                usable = min(s.prompt_len, s.prefill_target - 1) // self.block_size
+                hit = self.cache.match(s.prompt_tokens, usable)
+                self.bm.share(hit)
             try:
-                s.block_table = self.bm.allocate(self._blocks_for(s.prefill_target))
+                fresh = self._allocate(self._blocks_for(s.prefill_target) - len(hit))
             except OutOfBlocks:
+                if hit:
+                    self.bm.free(hit)
                 break
+            s.block_table = hit + fresh
+            s.computed = len(hit) * self.block_size
+            s.cached_tokens = s.computed
             self.waiting.pop(0)
             self.running.append(s)
             admitted += 1
@@ -181,16 +304,23 @@ class Scheduler:
             if budget is not None:
                 budget -= n
         self.iteration += 1
-        return self._pack(items, admitted, finished, preempted)
+        batch = self._pack(items, admitted, finished, preempted)
+        if self._copies:
+            batch.copies = np.array(self._copies, dtype=np.int32).reshape(-1, 2)
+            self._copies = []
+        return batch
 
     def complete(self, batch: IterationBatch) -> None:
-        """Account for the forward pass of `batch`: cache grows, decodes emit tokens."""
+        """Account for the forward pass of `batch`: cache grows, decodes emit tokens; with
+        the prefix cache, the prompt's newly completed full blocks become reusable."""
         for it in batch.items:
             s = it.seq
             was_decode = not s.in_prefill
             s.computed += it.q_len
             if was_decode:
                 s.decoded += 1
+            if self.cache is not None and s.prompt_tokens is not None and not was_decode:
+                self.cache.insert(s.prompt_tokens, s.block_table, min(s.computed, s.prompt_len) // self.block_size)
 
     def _pack(self, items, admitted, finished, preempted) -> IterationBatch:
         S = len(items)

@@ -264,6 +264,7 @@ class Request:
     arrival: int        # iteration index at which it joins the waiting queue
     prompt_len: int
     output_len: int
+    tokens: np.ndarray | None = None  # prompt token ids (shared-prefix workloads only)
 
 
 def request_stream(seed: int = 5001, iterations: int = 300, rate: float = 4.0,
@@ -283,6 +284,27 @@ def request_stream(seed: int = 5001, iterations: int = 300, rate: float = 4.0,
             p = min(max(p, 1), max_prompt)
             o = int(rng.integers(out_lo, out_hi + 1))
             reqs.append(Request(len(reqs), it, p, o))
+    return reqs
+
+
+def request_stream_shared_prefix(seed: int = 6001, iterations: int = 120, rate: float = 2.0,
+                                 num_prefixes: int = 3, vocab: int = 32000) -> list:
+    """Requests that share system prompts ("vLLM推理引擎架构PagedAttention机制与高吞吐推理"
+    (lpnh.cn) §4.3): num_prefixes system prompts of seeded lengths in [200, 1200] tokens;
+    each request = one of them + its own suffix of 1..400 tokens; token ids uniform in
+    [0, vocab).  Poisson(rate) arrivals per iteration, outputs uniform in [8, 64].
+    Each Request carries .tokens (int64 prompt ids)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    prefixes = [rng.integers(0, vocab, size=int(n)) for n in rng.integers(200, 1201, size=num_prefixes)]
+    reqs = []
+    rid = 0
+    for it in range(iterations):
+        for _ in range(int(rng.poisson(rate))):
+            p = prefixes[int(rng.integers(0, num_prefixes))]
+            suffix = rng.integers(0, vocab, size=int(rng.integers(1, 401)))
+            tokens = np.concatenate([p, suffix]).astype(np.int64)
+            reqs.append(Request(rid, it, len(tokens), int(rng.integers(8, 65)), tokens))
+            rid += 1
     return reqs
 
 

@@ -382,6 +382,59 @@ def pin_chunking_is_invisible(orc):
 
 
 # ---------------------------------------------------------------------------
+# Shared prefix blocks and copy-on-write ([LPNH] §4.3)
+# ---------------------------------------------------------------------------
+
+def pin_copy_blocks_worked_example(orc):
+    """A block copy makes block dst equal to block src in both caches and leaves every
+    other block, and the source, as they were."""
+    rng = _rng(95)
+    NB, bs, Hkv, d = 5, 16, 2, 8
+    kc = normal_bf16(rng, (NB, bs, Hkv, d))
+    vc = normal_bf16(rng, (NB, bs, Hkv, d))
+    k0, v0 = kc.copy(), vc.copy()
+    orc.copy_blocks(kc, vc, np.array([[3, 0], [1, 4]], np.int32))
+    assert np.array_equal(kc[0], k0[3]) and np.array_equal(vc[0], v0[3])
+    assert np.array_equal(kc[4], k0[1]) and np.array_equal(vc[4], v0[1])
+    for b in (1, 2, 3):
+        assert np.array_equal(kc[b], k0[b]) and np.array_equal(vc[b], v0[b])
+    try:
+        orc.copy_blocks(kc, vc, np.array([[0, NB]], np.int32))
+        raise AssertionError("a block id past the pool must be refused")
+    except ValueError:
+        pass
+
+
+def pin_shared_prefix_blocks_are_invisible(orc):
+    """[LPNH] §4.3: sequences that share a prompt prefix may point at the same read-only
+    blocks.  Their outputs equal those of sequences holding private copies of the
+    prefix, and the rows a sequence writes after the shared prefix stay its own."""
+    rng = _rng(96)
+    Hq, Hkv, d, bs = 8, 2, 16, 16
+    prefix_blocks = 3
+    ctx = [3 * bs + 5, 3 * bs + 16, 3 * bs + 1]
+    NB = 16
+    kc = normal_bf16(rng, (NB, bs, Hkv, d))
+    vc = normal_bf16(rng, (NB, bs, Hkv, d))
+    shared = np.array([2, 9, 5], np.int32)
+    own = [np.array([11], np.int32), np.array([0], np.int32), np.array([7], np.int32)]
+    tables_shared = np.stack([np.concatenate([shared, own[s]]) for s in range(3)])
+    # private copies of the prefix for each sequence
+    priv = [np.array([1, 3, 4], np.int32), np.array([6, 8, 10], np.int32), np.array([12, 13, 14], np.int32)]
+    kp, vp = kc.copy(), vc.copy()
+    for s in range(3):
+        for i in range(prefix_blocks):
+            kp[priv[s][i]] = kc[shared[i]]
+            vp[priv[s][i]] = vc[shared[i]]
+    tables_priv = np.stack([np.concatenate([priv[s], own[s]]) for s in range(3)])
+    q = normal_bf16(rng, (3, Hq, d))
+    cl = np.array(ctx, np.int32)
+    a = orc.paged_attention(q, kc, vc, tables_shared, cl, 0.3)
+    b = orc.paged_attention(q, kp, vp, tables_priv, cl, 0.3)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
 # FP8 cache (OCP 8-bit floating point, E4M3): the format's definition and
 # torch's float8_e4m3fn type (a library implementation of the same format)
 # ---------------------------------------------------------------------------

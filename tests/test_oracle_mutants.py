@@ -35,6 +35,11 @@ MUTANTS = [
     ("single_key_dropped", "if (n <= 0) {", "if (n <= 1) {"),
     ("exp_sign", "z[i] = exp(z[i] - m);", "z[i] = exp(m - z[i]);"),
     ("max_is_min", "if (z[i] > m) m = z[i];", "if (z[i] < m) m = z[i];"),
+    # block copy
+    ("copy_swapped", "k_cache[dst * block_bytes + b] = k_cache[src * block_bytes + b];",
+     "k_cache[src * block_bytes + b] = k_cache[dst * block_bytes + b];"),
+    ("copy_v_from_k", "v_cache[dst * block_bytes + b] = v_cache[src * block_bytes + b];",
+     "v_cache[dst * block_bytes + b] = k_cache[src * block_bytes + b];"),
     # FP8 (e4m3) cache
     ("e4m3_bias_8", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
     ("e4m3_subnormal_step", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
