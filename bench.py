@@ -50,6 +50,8 @@ def parse():
                    choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen", "cb_trace",
                             "gqa_decode_fp8"])
     p.add_argument("--seed", type=int, default=None)
+    p.add_argument("--block-size", type=int, default=16,
+                   help="tokens per pool block for the decode workloads (8, 16, 32, 64)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -76,8 +78,15 @@ WORKLOADS = {
 }
 
 
-def make_batch(config, seed):
+def make_batch(config, seed, block_size=16):
     from pagedattention_paged_kv_gb300 import workloads as W
+    if block_size != 16:
+        if config not in ("gqa_decode", "gqa_decode_fp8", "skewed_decode"):
+            raise SystemExit("--block-size applies to the decode workloads only")
+        if config == "gqa_decode_fp8":
+            return W.to_fp8_pool(W.gqa_decode(seed=seed, block_size=block_size))
+        return {"gqa_decode": W.gqa_decode, "skewed_decode": W.skewed_decode}[config](
+            seed=seed, block_size=block_size)
     if config == "gqa_decode_fp8":
         return W.to_fp8_pool(W.gqa_decode(seed=seed))
     return {"gqa_decode": W.gqa_decode, "tiny_decode": W.tiny_decode,
@@ -106,13 +115,21 @@ def algorithmic_bytes(b):
     """(step bytes, attention-call bytes): every context row of K and V once, the
     queries and outputs once, the new K/V rows read and written once, block-table
     entries, context lengths and slots read once."""
-    nblk = int(((b.context_lens.astype(np.int64) + 15) // 16).sum())
+    nblk = int(((b.context_lens.astype(np.int64) + b.block_size - 1) // b.block_size).sum())
     attn = kv_bytes(b) + 2 * b.q.size * 2 + nblk * 4 + b.num_seqs * 4
     if b.query_start_loc is not None:
         attn += (b.num_seqs + 1) * 4
     elem = 1 if is_fp8(b) else 2
     new = 2 * b.k_new.size * 2 + 2 * b.k_new.size * elem + b.k_new.shape[0] * 8  # read bf16, write cache
     return attn + new, attn
+
+
+def slot_waste(b):
+    """Share of the sequences' block slots that hold no token ([LPNH] §4.1: the cost of
+    larger blocks)."""
+    ctx = b.context_lens.astype(np.int64)
+    slots = ((ctx + b.block_size - 1) // b.block_size * b.block_size).sum()
+    return float((slots - ctx.sum()) / max(1, slots))
 
 
 def chunk_flops(context_lens, q_lens, head_dim, num_heads):
@@ -271,7 +288,7 @@ def run_reference(args, rank):
     if rank != 0:
         return
     seed = args.seed if args.seed is not None else WORKLOADS[args.config][1]
-    b = make_batch(args.config, seed)
+    b = make_batch(args.config, seed, args.block_size)
     total, _ = algorithmic_bytes(b)
     seqs = sample_seqs(b, 16)
     warmup = min(args.warmup, 1)   # the oracle has no caches to warm; one untimed run
@@ -407,7 +424,7 @@ def main():
     seed = (args.seed if args.seed is not None else default_seed) + rank
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    b = make_batch(args.config, seed)
+    b = make_batch(args.config, seed, args.block_size)
     varlen = b.query_start_loc is not None
     total_bytes, attn_bytes = algorithmic_bytes(b)
     S, Hq, d = b.num_seqs, b.num_heads, b.head_dim
@@ -533,7 +550,8 @@ def main():
         "dtype": "fp8_e4m3 kv / f16 mma / f32 acc" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random block permutation" +
                 ("; pool = e4m3 codes of x / scale)" if fp8 else ")"),
-        "config": {"workload": name, **cfg, "seed": seed,
+        "config": {"workload": name, **cfg, "seed": seed, "block_size": b.block_size,
+                   "slot_waste": slot_waste(b),
                    "sum_context": int(b.context_lens.astype(np.int64).sum()), "num_blocks": b.num_blocks,
                    "parallelism": f"replicas x{world}",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write); KV pool "

@@ -101,7 +101,9 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, in
     cuuint64_t dims[5] = {(cuuint64_t)cw, (cuuint64_t)block_size, (cuuint64_t)num_kv_heads,
                           (cuuint64_t)(head_dim / cw), (cuuint64_t)num_blocks};
     cuuint64_t strides[4] = {row, (cuuint64_t)head_dim * elem, 128, row * block_size};
-    cuuint32_t box[5] = {(cuuint32_t)cw, (cuuint32_t)block_size, (cuuint32_t)box_heads, 1, 1};
+    // a box is one 16-token slice of a block (block sizes >= 16) or one whole 8-token block
+    const cuuint32_t box_tokens = block_size < 16 ? (cuuint32_t)block_size : 16u;
+    cuuint32_t box[5] = {(cuuint32_t)cw, box_tokens, (cuuint32_t)box_heads, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
                           const_cast<void *>(cache), dims,
@@ -175,7 +177,9 @@ int check_common(int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv
         return PKV_ERR_INVALID_ARG;
     if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
-    if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    // decode: pool blocks of 8, 16, 32 or 64 tokens (prefill rows need 16, checked there)
+    if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64)
+        return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_blocks * block_size > (int64_t)UINT32_MAX) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * max_blocks_per_seq * num_kv_heads > (int64_t)INT32_MAX)
@@ -189,16 +193,17 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
                const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
                int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
                int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
-               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, bool fp8 = false,
-               float k_scale = 1.f, float v_scale = 1.f) {
+               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, int block_size,
+               bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
     if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
     CUtensorMap kmap, vmap;
-    int st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
-                              p.heads_per_cta, fp8);
+    const int box_heads = block_size < kBlockSize ? 1 : p.heads_per_cta;
+    int st = encode_cache_map(&kmap, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box_heads,
+                              fp8);
     if (st == PKV_OK)
-        st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim,
-                              p.heads_per_cta, fp8);
+        st = encode_cache_map(&vmap, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box_heads,
+                              fp8);
     if (st != PKV_OK) return st;
     pkv::DecodeArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -209,6 +214,7 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     a.total_q = total_q;
     a.num_seqs = num_seqs;
     a.max_blocks_per_seq = max_blocks_per_seq;
+    a.block_size = block_size;
     a.num_heads = num_heads;
     a.group = p.group;
     a.heads_per_cta = p.heads_per_cta;
@@ -370,7 +376,7 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *q, const void *
     return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens, num_seqs,
                       max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
                       static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), block_size);
 }
 
 extern "C" int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
@@ -401,7 +407,7 @@ extern "C" int pkv_paged_attention_decode_fp8(void *out, const void *q, const vo
     return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens, num_seqs,
                       max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
                       static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
-                      static_cast<cudaStream_t>(stream), true, k_scale, v_scale);
+                      static_cast<cudaStream_t>(stream), block_size, true, k_scale, v_scale);
 }
 
 extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
@@ -431,6 +437,7 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     if (st != PKV_OK) return st;
     pkv::PrefillPlan pp;
     const bool prefill_rows = max_q_len >= 2;
+    if (prefill_rows && block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
     if (prefill_rows) {
         st = pkv::plan_prefill(num_seqs, num_heads, num_kv_heads, head_dim, d->sms, d->smem_optin,
                                &pp);
@@ -443,7 +450,7 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     // Single-token rows: the decode kernel (it skips every other sequence).
     st = run_decode(out, q, query_start_loc, total_q_tokens, k_cache, v_cache, block_tables, context_lens,
                     num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
-                    scale, ws, p.bytes, *d, p, s);
+                    scale, ws, p.bytes, *d, p, s, block_size);
     if (st != PKV_OK || !prefill_rows) return st;
     // Multi-token rows (prefill chunks): the chunked-prefill kernel.
     CUtensorMap qmap, kmap, vmap;
@@ -540,5 +547,5 @@ extern "C" int pkv_paged_attention_decode_static(void *out, const void *q, const
     return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens,
                       num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
                       scale, static_cast<uint8_t *>(scratch), PKV_STATIC_SCRATCH_BYTES, *d, p,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), block_size);
 }

@@ -34,7 +34,10 @@ namespace pkv {
 
 namespace {
 
-constexpr int kBS = 16;  // tokens per block (the fast path's block size)
+// The kernel's unit of work is a 16-token slice of a sequence ("unit"); a pool block of
+// block_size tokens holds block_size / 16 units (block sizes 16, 32, 64) or half of one
+// (block size 8: a unit's two halves come from two pool blocks).
+constexpr int kBS = 16;
 
 // Blocks of KV the work item (virtual sequence) v contributes.
 __device__ __forceinline__ int32_t item_blocks(const DecodeArgs &a, int v, bool report) {
@@ -52,7 +55,7 @@ __device__ __forceinline__ int32_t item_blocks(const DecodeArgs &a, int v, bool 
             return 0;
         }
     }
-    if (ctx < 0 || (int64_t)ctx > (int64_t)a.max_blocks_per_seq * kBS) {
+    if (ctx < 0 || (int64_t)ctx > (int64_t)a.max_blocks_per_seq * a.block_size) {
         if (report) flag_error(a.err, PKV_DEVERR_CONTEXT_LEN);
         return 0;
     }
@@ -207,24 +210,38 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         uint32_t stage = 0, phase = 0;
         uint32_t issued = 0;
         bool ok = true;
+        const int bsz = a.block_size;
+        auto checked = [&](int id) {
+            if (id < 0 || (int64_t)id >= a.num_blocks) {
+                flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                return -1;  // TMA fills the out-of-range box with zeros
+            }
+            return id;
+        };
         for (int64_t f0 = lo; f0 < hi && ok; f0 += 32) {
             const int64_t f = f0 + lane;
-            int bid = -1, ht = 0;
+            int bid = -1, bid2 = -1, ht = 0, tok0 = 0;
             if (f < hi) {
                 const int v = find_item(pre, V, f);
                 const int s = v / a.head_tiles;
                 ht = v - s * a.head_tiles;
-                const int lb = (int)(f - pre[v]);
-                bid = a.block_tables[(int64_t)s * a.max_blocks_per_seq + lb];
-                if (bid < 0 || (int64_t)bid >= a.num_blocks) {
-                    flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                    bid = -1;  // TMA fills the out-of-range box with zeros
+                const int lb = (int)(f - pre[v]);  // unit inside the sequence
+                const int32_t *row = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
+                if (bsz >= kBS) {
+                    const int r = bsz / kBS;
+                    bid = checked(row[lb / r]);
+                    tok0 = (lb % r) * kBS;
+                } else {  // 8-token blocks: the unit's second half exists only inside the context
+                    bid = checked(row[2 * lb]);
+                    if (2 * lb + 1 < (a.context_lens[s] + bsz - 1) / bsz) bid2 = checked(row[2 * lb + 1]);
                 }
             }
             const int n = (int)min64(32, hi - f0);
             for (int j = 0; j < n; ++j) {
                 const int b = __shfl_sync(0xffffffffu, bid, j);
+                const int b2 = __shfl_sync(0xffffffffu, bid2, j);
                 const int t = __shfl_sync(0xffffffffu, ht, j);
+                const int tk = __shfl_sync(0xffffffffu, tok0, j);
                 if (lane == 0) {
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
@@ -235,10 +252,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                         mbar_arrive_expect_tx(&full[stage], stage_bytes);
                         uint8_t *dst = smem + (size_t)stage * stage_bytes;
                         const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
+                        if (bsz >= kBS) {
 #pragma unroll
-                        for (int dc = 0; dc < DCH; ++dc)
-                            tma_load_5d(dst + dc * chunk_stride, map, &full[stage], 0, 0, t * HT,
-                                        dc, b, policy);
+                            for (int dc = 0; dc < DCH; ++dc)
+                                tma_load_5d(dst + dc * chunk_stride, map, &full[stage], 0, tk, t * HT,
+                                            dc, b, policy);
+                        } else {
+                            // one 8-token box per head and half: each head's 16 rows stay
+                            // contiguous (the swizzle follows the shared-memory address)
+                            for (int dc = 0; dc < DCH; ++dc)
+                                for (int h = 0; h < HT; ++h)
+                                    for (int half = 0; half < 2; ++half)
+                                        tma_load_5d(dst + dc * chunk_stride + h * (kBS * 128) + half * (8 * 128),
+                                                    map, &full[stage], 0, 0, t * HT + h, dc, half ? b2 : b,
+                                                    policy);
+                        }
                         ++issued;
                         if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
                     }

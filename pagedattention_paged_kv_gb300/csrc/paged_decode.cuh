@@ -18,6 +18,7 @@ struct DecodeArgs {
     int total_q;                     // rows of q and out
     int num_seqs;
     int max_blocks_per_seq;
+    int block_size;      // tokens per pool block: 8, 16, 32 or 64
     int num_heads;
     int group;           // num_heads / num_kv_heads
     int heads_per_cta;   // KV heads per work item
