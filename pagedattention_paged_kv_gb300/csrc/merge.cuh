@@ -8,8 +8,8 @@
 //
 // The main kernel's CTA 0 writes one MergeJob per boundary between neighbouring CTA
 // shares (the item split there, if that boundary is the item's first split); the merge
-// kernel runs one CTA row-slice per job, so a job costs three rounds of global loads
-// (job, (m, l) of its parts, o of its parts) whatever the batch.
+// kernel runs one CTA per 16 rows of a job, so a job costs three rounds of global loads
+// (job, (m, l) of its parts, o of its parts) whatever the batch and however many parts.
 #pragma once
 
 #include "attn_block.cuh"
@@ -37,8 +37,8 @@ struct MergeArgs {
     int num_heads;
 };
 
-constexpr int kMergeMaxRows = 16;    // rows per CTA; a job gets ceil(slot_rows / 16) CTAs
-constexpr int kMergeSmemParts = 32;  // parts whose (m, l) and weight stay in shared memory
+constexpr int kMergeRows = 16;       // rows per CTA; a job gets ceil(slot_rows / 16) CTAs
+constexpr int kMergeMaxParts = 256;  // the grids hold <= 256 CTAs, so an item has <= 256 parts
 
 __device__ __forceinline__ void no_job(MergeJob &j) {
     j.item_begin = j.total_units = j.out_row0 = 0;
@@ -46,76 +46,134 @@ __device__ __forceinline__ void no_job(MergeJob &j) {
     j.ge = j.rows = j.rows_per_token = j.head0 = 0;
 }
 
+// Three rounds of global loads per CTA (the job; (m, l) of its rows' parts; o of its
+// rows' parts).  The 8 warps split the (row, part) pairs: G = min(8, parts) part groups
+// (a power of two) times 8 / G row groups, so a job split into many parts keeps every warp
+// busy with independent loads and a two-part job still uses all warps.  The part groups'
+// sums are added in group order (bit-reproducible).
 template <int D>
-__global__ void __launch_bounds__(256) merge_parts_kernel(const MergeArgs m) {
-    __shared__ float2 s_ml[kMergeMaxRows][kMergeSmemParts];
-    __shared__ float s_base[kMergeMaxRows], s_inv[kMergeMaxRows];
+__global__ void __launch_bounds__(256, 4) merge_parts_kernel(const MergeArgs m) {
+    constexpr int D4 = D / 4;
+    __shared__ float s_w[kMergeRows][kMergeMaxParts];  // m_p, then the weight 2^(m_p - M)
+    __shared__ float s_inv[kMergeRows];
+    __shared__ float4 s_acc[kMergeRows][D4];
     pdl_wait();
     const MergeJob j = m.jobs[blockIdx.x];
     if (j.c0 < 0) return;
     const int nparts = j.c1 - j.c0 + 1;
-    const int np_s = nparts < kMergeSmemParts ? nparts : kMergeSmemParts;
-    const int y = blockIdx.y, ny = gridDim.y;  // rows y, y + ny, y + 2 ny, ...
-    const int my_rows = (j.rows - y + ny - 1) / ny;
-    if (my_rows <= 0) return;
-    // (m, l) of my rows x the first parts, all loads in flight together
-    for (int i = threadIdx.x; i < my_rows * np_s; i += blockDim.x) {
-        const int k = i / np_s, p = i - k * np_s;
-        const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
-        s_ml[k][p] = m.ws_ml[(int64_t)slot * m.slot_rows + y + k * ny];
-    }
-    __syncthreads();
-    for (int k = threadIdx.x; k < my_rows; k += blockDim.x) {
-        const int row = y + k * ny;
-        float M = -INFINITY;
-        for (int p = 0; p < nparts; ++p)
-            M = fmaxf(M, p < np_s ? s_ml[k][p].x
-                                  : m.ws_ml[(int64_t)part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge) *
-                                                m.slot_rows + row].x);
+    const int row0 = blockIdx.y * kMergeRows;
+    if (row0 >= j.rows || nparts > kMergeMaxParts) return;
+    const int nrows = min(kMergeRows, j.rows - row0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // (1) warp w: the weights of rows w and w + 8
+    for (int k = warp; k < nrows; k += 8) {
+        const int row = row0 + k;
+        float M = -INFINITY, lv[kMergeMaxParts / 32];
+#pragma unroll
+        for (int i = 0; i < kMergeMaxParts / 32; ++i) {
+            const int p = lane + 32 * i;
+            lv[i] = 0.f;
+            if (p < nparts) {
+                const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
+                const float2 ml = m.ws_ml[(int64_t)slot * m.slot_rows + row];
+                s_w[k][p] = ml.x;
+                lv[i] = ml.y;
+                M = fmaxf(M, ml.x);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         const float base = M == -INFINITY ? 0.f : M;  // rows that saw nothing keep weight 0
         float L = 0.f;
-        for (int p = 0; p < nparts; ++p) {
-            const float2 ml = p < np_s ? s_ml[k][p]
-                                       : m.ws_ml[(int64_t)part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge) *
-                                                     m.slot_rows + row];
-            const float w = fast_exp2(ml.x - base);
-            L += w * ml.y;
-            if (p < np_s) s_ml[k][p].x = w;  // keep the weight in place of m
+#pragma unroll
+        for (int i = 0; i < kMergeMaxParts / 32; ++i) {
+            const int p = lane + 32 * i;
+            if (p < nparts) {
+                const float w = fast_exp2(s_w[k][p] - base);
+                s_w[k][p] = w;
+                L += w * lv[i];
+            }
         }
-        s_base[k] = base;
-        s_inv[k] = 1.f / L;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) s_inv[k] = 1.f / L;
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
-    for (int task = threadIdx.x; task < my_rows * D4; task += blockDim.x) {
-        const int k = task / D4, d4 = task - k * D4;
-        const int row = y + k * ny;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int p = 0; p < nparts; ++p) {
-            const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
-            const float w = p < np_s ? s_ml[k][p].x
-                                     : fast_exp2(m.ws_ml[(int64_t)slot * m.slot_rows + row].x - s_base[k]);
-            const float4 ov = reinterpret_cast<const float4 *>(m.ws_o + ((int64_t)slot * m.slot_rows + row) * D)[d4];
-            acc.x += w * ov.x;
-            acc.y += w * ov.y;
-            acc.z += w * ov.z;
-            acc.w += w * ov.w;
+    // (2) warp w = (row group rg, part group pg): rows rg, rg + RG, ...; parts pg, pg + G, ...
+    const int G = nparts >= 8 ? 8 : nparts >= 4 ? 4 : nparts >= 2 ? 2 : 1;
+    const int RG = 8 / G;
+    const int pg = warp % G, rg = warp / G;
+    static_assert(D4 <= 32, "one lane per 4 columns");
+    const int d4 = lane;
+    const bool col = d4 < D4;
+    // rows in passes of 4 per warp (few registers: the CTA then fits next to the tail of
+    // the kernel that produced the parts)
+    for (int r0 = 0; r0 < nrows; r0 += 4 * RG) {
+        float4 acc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col) {
+#pragma unroll 2
+            for (int p = pg; p < nparts; p += G) {
+                const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
+                const float4 *ob =
+                    reinterpret_cast<const float4 *>(m.ws_o + ((int64_t)slot * m.slot_rows + row0) * D);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int k = r0 + rg + i * RG;
+                    if (k < nrows) {
+                        const float w = s_w[k][p];
+                        const float4 ov = ob[k * D4 + d4];
+                        acc[i].x += w * ov.x;
+                        acc[i].y += w * ov.y;
+                        acc[i].z += w * ov.z;
+                        acc[i].w += w * ov.w;
+                    }
+                }
+            }
         }
+        // (3) add the part groups in order: group 0 stores, groups 1 .. G-1 add in turn
+        // (every thread takes every barrier)
+        for (int g = 0; g < G; ++g) {
+            if (pg == g && col) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int k = r0 + rg + i * RG;
+                    if (k < nrows) {
+                        if (g == 0) {
+                            s_acc[k][d4] = acc[i];
+                        } else {
+                            float4 t = s_acc[k][d4];
+                            t.x += acc[i].x;
+                            t.y += acc[i].y;
+                            t.z += acc[i].z;
+                            t.w += acc[i].w;
+                            s_acc[k][d4] = t;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // (4) one thread per (row, 4 columns): normalise, store bf16
+    for (int idx = threadIdx.x; idx < nrows * D4; idx += blockDim.x) {
+        const int k = idx / D4, d4 = idx - k * D4;
+        const float4 t = s_acc[k][d4];
         const float inv = s_inv[k];
+        const int row = row0 + k;
         const int tok = row / j.rows_per_token, hr = row - tok * j.rows_per_token;
-        __nv_bfloat16 *orow =
-            m.out + ((j.out_row0 + tok) * (int64_t)m.num_heads + j.head0 + hr) * D;
+        __nv_bfloat16 *orow = m.out + ((j.out_row0 + tok) * (int64_t)m.num_heads + j.head0 + hr) * D;
         uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        packed.x = pack_bf16x2(t.x * inv, t.y * inv);
+        packed.y = pack_bf16x2(t.z * inv, t.w * inv);
         reinterpret_cast<uint2 *>(orow)[d4] = packed;
     }
 }
 
 template <int D>
 cudaError_t launch_merge(const MergeArgs &m, int grid, cudaStream_t stream) {
-    const int ny = (m.slot_rows + kMergeMaxRows - 1) / kMergeMaxRows;
+    const int ny = (m.slot_rows + kMergeRows - 1) / kMergeRows;
     return launch_pdl(merge_parts_kernel<D>, dim3(grid, ny), dim3(256), 0, stream, m);
 }
 
