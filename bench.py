@@ -54,6 +54,8 @@ def parse():
                    help="tokens per pool block for the decode workloads (8, 16, 32, 64)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--separate-kv-write", action="store_true",
+                   help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
 
 
@@ -462,12 +464,21 @@ def main():
         if varlen:
             pkv.paged_attention_varlen(o, qq, qs, kc, vc, tables, lens, b.scale, causal=b.causal,
                                        max_q_len=max_q_len, workspace=ws)
+        elif fused:
+            kw = {"k_scale": ks, "v_scale": vs} if fp8 else {}
+            pkv.paged_attention_decode_kvwrite(o, qq, k_new, v_new, kc, vc, tables, lens, b.scale, workspace=ws, **kw)
         elif fp8:
             pkv.paged_attention_decode_fp8(o, qq, kc, vc, tables, lens, b.scale, ks, vs, workspace=ws)
         else:
             pkv.paged_attention_decode(o, qq, kc, vc, tables, lens, b.scale, workspace=ws)
 
+    # decode steps run the KV write inside the decode launch (one new row per sequence)
+    fused = not varlen and not args.separate_kv_write and b.k_new.shape[0] == S \
+        and np.array_equal(b.new_token_seq, np.arange(S)) and np.array_equal(b.new_token_pos, b.context_lens - 1)
+
     def kv_write():
+        if fused:
+            return
         if fp8:
             pkv.reshape_and_cache_fp8(kc, vc, k_new, v_new, sm, ks, vs)
         else:
@@ -518,8 +529,13 @@ def main():
             attention()
             hout.copy_(out, non_blocking=True)
 
+        def host_slots():
+            # the fused decode step derives the new token's slot on the device
+            if not fused:
+                h_slots[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+
         def eager_step():
-            h_slots[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+            host_slots()
             device_part()
             stream.synchronize()
 
@@ -530,7 +546,7 @@ def main():
             cap = CapturedStep(device_part)
 
             def graph_step():
-                h_slots[:] = pkv.slot_mapping(b.block_tables, b.new_token_seq, b.new_token_pos, b.block_size)
+                host_slots()
                 cap.replay()
                 cap.synchronize()
         except Exception as exc:  # capture not available: report the eager path only
@@ -574,7 +590,7 @@ def main():
 
     if rank != 0:
         return
-    launches_per_step = 1 + (2 if not varlen else (4 if max_q_len >= 2 else 2))
+    launches_per_step = (0 if fused else 1) + (2 if not varlen else (4 if max_q_len >= 2 else 2))
     line = {
         "metric": METRIC if args.config == "gqa_decode" else f"{name}: HBM GB/s of the step",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -592,6 +608,7 @@ def main():
         "seq_steps_per_s": S * world / (t_step * 1e-3),
         "algorithmic_bytes_per_step": total_bytes,
         "kv_write_us": 1e3 * sum(kv_ms) / len(kv_ms),
+        "kv_write": "fused into the decode launch" if fused else "separate launch",
         "attention_us": 1e3 * t_attn,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),

@@ -159,6 +159,34 @@ int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * Decode step with its KV write fused into the attention launch.  For every sequence s
+ * with context_lens[s] >= 1, the rows k_new[s] and v_new[s] (k_new, v_new [num_seqs,
+ * num_kv_heads, head_dim] bf16, device) are stored at position p = context_lens[s] - 1
+ * -- block block_tables[s][p / block_size], offset p % block_size -- and then
+ * out[s] = decode attention over positions 0 .. p, exactly as pkv_slot_mapping of those
+ * positions + pkv_reshape_and_cache (resp. pkv_reshape_and_cache_fp8) +
+ * pkv_paged_attention_decode (resp. _fp8) would give, in one launch (plus the merge).
+ * The thread block that reads a sequence's last 16 positions writes its new rows first.
+ * Arguments, support and errors as for pkv_paged_attention_decode (dtype must be
+ * PKV_DTYPE_BF16) and pkv_paged_attention_decode_fp8; k_new and v_new 16-byte aligned.
+ * A block id outside the pool at position p skips that write (PKV_DEVERR_BLOCK_ID).
+ */
+int pkv_paged_attention_decode_kvwrite(void *out, const void *q, const void *k_new, const void *v_new,
+                                       void *k_cache, void *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                                       int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                       int64_t num_blocks, float scale, int dtype, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+int pkv_paged_attention_decode_kvwrite_fp8(void *out, const void *q, const void *k_new,
+                                           const void *v_new, void *k_cache, void *v_cache,
+                                           const int32_t *block_tables, const int32_t *context_lens,
+                                           int num_seqs, int max_blocks_per_seq, int num_heads,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int64_t num_blocks, float scale, float k_scale,
+                                           float v_scale, void *workspace, size_t workspace_bytes,
+                                           void *stream);
+
+/*
  * Block copy (the device half of copy-on-write, [LPNH] §4.3): for each i < num_pairs,
  * with (src, dst) = (block_pairs[2i], block_pairs[2i+1]) (device int32),
  *     k_cache[dst] = k_cache[src]  and  v_cache[dst] = v_cache[src]   (whole blocks)

@@ -67,6 +67,10 @@ def lib() -> ctypes.CDLL:
         L.pkv_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      i32, i64, f32, f32, f32, vp, sz, vp]
         L.pkv_copy_blocks.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        L.pkv_paged_attention_decode_kvwrite.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                         i32, i32, i64, f32, i32, vp, sz, vp]
+        L.pkv_paged_attention_decode_kvwrite_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                             i32, i32, i32, i64, f32, f32, f32, vp, sz, vp]
         L.pkv_block_manager_share.argtypes = [vp, vp, i64]
         L.pkv_block_manager_ref_count.argtypes = [vp, ctypes.c_int32]
         L.pkv_block_manager_copy_on_write.argtypes = [vp, ctypes.c_int32, vp]
@@ -88,7 +92,8 @@ def lib() -> ctypes.CDLL:
                      "pkv_paged_attention_varlen", "pkv_get_device_error", "pkv_slot_mapping",
                      "pkv_block_manager_allocate", "pkv_block_manager_free", "pkv_copy_blocks",
                      "pkv_block_manager_share", "pkv_block_manager_ref_count",
-                     "pkv_block_manager_copy_on_write"):
+                     "pkv_block_manager_copy_on_write", "pkv_paged_attention_decode_kvwrite",
+                     "pkv_paged_attention_decode_kvwrite_fp8"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -258,6 +263,41 @@ def paged_attention_varlen(out, q, query_start_loc, k_cache, v_cache, block_tabl
         _ptr(block_tables), _ptr(context_lens), S, total_q, int(max_q_len), block_tables.shape[1],
         Hq, Hkv, d, bs, NB, float(scale), int(bool(causal)), DTYPE_BF16, _ptr(ws),
         ws.numel() * ws.element_size(), _stream_ptr(stream)), "paged_attention_varlen")
+
+
+def paged_attention_decode_kvwrite(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                                   scale: float, k_scale: float | None = None, v_scale: float | None = None,
+                                   workspace=None, stream=None) -> None:
+    """Decode step with the KV write fused in: k_new/v_new [S, Hkv, d] bf16 rows go to position
+    context_lens[s] - 1, then out = decode attention.  A uint8 (e4m3) cache needs k_scale and
+    v_scale; a bf16 cache takes none."""
+    import torch
+    fp8 = k_cache.dtype == torch.uint8
+    _require(out, torch.bfloat16, "out", 3)
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_new, torch.bfloat16, "k_new", 3)
+    _require(v_new, torch.bfloat16, "v_new", 3)
+    _require(k_cache, torch.uint8 if fp8 else torch.bfloat16, "k_cache", 4)
+    _require(v_cache, k_cache.dtype, "v_cache", 4)
+    _require(block_tables, torch.int32, "block_tables", 2)
+    _require(context_lens, torch.int32, "context_lens", 1)
+    S, Hq, d = q.shape
+    NB, bs, Hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != S \
+            or context_lens.shape[0] != S or tuple(k_new.shape) != (S, Hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch")
+    if fp8 and (k_scale is None or v_scale is None):
+        raise ValueError("an FP8 cache needs k_scale and v_scale")
+    nbytes = workspace_size(OP_DECODE, S, S, Hq, Hkv, d, bs)
+    ws = _workspace(workspace, nbytes, q.device)
+    args = [_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), S, block_tables.shape[1], Hq, Hkv, d, bs, NB, float(scale)]
+    tail = [_ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)]
+    if fp8:
+        _check(lib().pkv_paged_attention_decode_kvwrite_fp8(*args, float(k_scale), float(v_scale), *tail),
+               "paged_attention_decode_kvwrite_fp8")
+    else:
+        _check(lib().pkv_paged_attention_decode_kvwrite(*args, DTYPE_BF16, *tail), "paged_attention_decode_kvwrite")
 
 
 def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:

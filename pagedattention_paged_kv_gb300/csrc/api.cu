@@ -194,7 +194,8 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
                int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
                int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
                const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, int block_size,
-               bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+               bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f, const void *k_new = nullptr,
+               const void *v_new = nullptr) {
     if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
     CUtensorMap kmap, vmap;
@@ -226,6 +227,12 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     a.num_blocks = num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f * k_scale;
     a.v_scale = v_scale;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache_w = const_cast<void *>(k_cache);
+    a.v_cache_w = const_cast<void *>(v_cache);
+    a.k_scale_q = k_scale;
+    a.v_scale_q = v_scale;
     a.ws_jobs = reinterpret_cast<pkv::MergeJob *>(ws + p.off_jobs);
     a.ws_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
     a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
@@ -408,6 +415,68 @@ extern "C" int pkv_paged_attention_decode_fp8(void *out, const void *q, const vo
                       max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
                       static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
                       static_cast<cudaStream_t>(stream), block_size, true, k_scale, v_scale);
+}
+
+// Decode with the step's KV write fused in (bf16 or FP8 cache); see pagedkv.h.
+static int decode_kvwrite(void *out, const void *q, const void *k_new, const void *v_new, void *k_cache,
+                          void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_blocks, float scale, bool fp8,
+                          float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, PKV_DTYPE_BF16);
+    if (st != PKV_OK) return st;
+    if (fp8) {
+        if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+        if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
+            return PKV_ERR_INVALID_ARG;
+    }
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(k_new, 16) || !aligned(v_new, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    st = device_info(&d);
+    if (st != PKV_OK) return st;
+    DecodePlan p;
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p, fp8 ? 1 : 2);
+    if (st != PKV_OK) return st;
+    return run_decode(out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks, scale,
+                      static_cast<uint8_t *>(workspace), workspace_bytes, *d, p,
+                      static_cast<cudaStream_t>(stream), block_size, fp8, fp8 ? k_scale : 1.f,
+                      fp8 ? v_scale : 1.f, k_new, v_new);
+}
+
+extern "C" int pkv_paged_attention_decode_kvwrite(void *out, const void *q, const void *k_new,
+                                                  const void *v_new, void *k_cache, void *v_cache,
+                                                  const int32_t *block_tables, const int32_t *context_lens,
+                                                  int num_seqs, int max_blocks_per_seq, int num_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int64_t num_blocks, float scale, int dtype,
+                                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    return decode_kvwrite(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                          max_blocks_per_seq, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          scale, false, 1.f, 1.f, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_paged_attention_decode_kvwrite_fp8(void *out, const void *q, const void *k_new,
+                                                      const void *v_new, void *k_cache, void *v_cache,
+                                                      const int32_t *block_tables,
+                                                      const int32_t *context_lens, int num_seqs,
+                                                      int max_blocks_per_seq, int num_heads,
+                                                      int num_kv_heads, int head_dim, int block_size,
+                                                      int64_t num_blocks, float scale, float k_scale,
+                                                      float v_scale, void *workspace,
+                                                      size_t workspace_bytes, void *stream) {
+    return decode_kvwrite(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                          max_blocks_per_seq, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                          scale, true, k_scale, v_scale, workspace, workspace_bytes, stream);
 }
 
 extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,

@@ -26,6 +26,7 @@
 //    reports PKV_DEVERR_TIMEOUT instead of hanging.
 #include "attn_block.cuh"
 #include "fp8_block.cuh"
+#include "kv_quant.cuh"
 #include "merge.cuh"
 #include "paged_decode.cuh"
 #include "pkv_split.cuh"
@@ -218,15 +219,35 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             }
             return id;
         };
+        const int Hkv = a.num_heads / a.group;
         for (int64_t f0 = lo; f0 < hi && ok; f0 += 32) {
             const int64_t f = f0 + lane;
             int bid = -1, bid2 = -1, ht = 0, tok0 = 0;
+            int64_t wslot = -1;  // fused KV write: slot of the new token if this is its unit
+            int wseq = 0;
             if (f < hi) {
                 const int v = find_item(pre, V, f);
                 const int s = v / a.head_tiles;
                 ht = v - s * a.head_tiles;
                 const int lb = (int)(f - pre[v]);  // unit inside the sequence
                 const int32_t *row = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
+                if (a.k_new && f == pre[v + 1] - 1) {
+                    const int p = a.context_lens[s] - 1;  // the new token's position
+                    const int nb = checked(row[p / bsz]);
+                    if (nb >= 0) {
+                        wslot = (int64_t)nb * bsz + p % bsz;
+                        wseq = s;
+                        // pull the new rows into L2 now: the copy below runs when the unit
+                        // comes up, up to 32 units later
+                        const int64_t src = ((int64_t)s * Hkv + (int64_t)ht * HT) * D * 2;
+                        const char *kp = static_cast<const char *>(a.k_new) + src;
+                        const char *vp = static_cast<const char *>(a.v_new) + src;
+                        for (int off = 0; off < HT * D * 2; off += 128) {
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(kp + off));
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(vp + off));
+                        }
+                    }
+                }
                 if (bsz >= kBS) {
                     const int r = bsz / kBS;
                     bid = checked(row[lb / r]);
@@ -242,6 +263,42 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                 const int b2 = __shfl_sync(0xffffffffu, bid2, j);
                 const int t = __shfl_sync(0xffffffffu, ht, j);
                 const int tk = __shfl_sync(0xffffffffu, tok0, j);
+                const int64_t ws = __shfl_sync(0xffffffffu, wslot, j);
+                if (ws >= 0) {
+                    // The unit holds its sequence's new token: store the token's K and V rows
+                    // for this item's heads (the whole warp), then order those stores before
+                    // the TMA reads of the unit (async proxy) issued below.
+                    const int sj = __shfl_sync(0xffffffffu, wseq, j);
+                    const int64_t dst_off = ws * Hkv + (int64_t)t * HT;   // in head rows
+                    const int64_t src_off = (int64_t)sj * Hkv + (int64_t)t * HT;
+                    if constexpr (FP8) {
+                        constexpr int V16 = D / 16;  // 16-code vectors per head row
+                        const uint4 *ks = reinterpret_cast<const uint4 *>(a.k_new) + src_off * (D / 8);
+                        const uint4 *vs = reinterpret_cast<const uint4 *>(a.v_new) + src_off * (D / 8);
+                        uint4 *kd = reinterpret_cast<uint4 *>(a.k_cache_w) + dst_off * V16;
+                        uint4 *vd = reinterpret_cast<uint4 *>(a.v_cache_w) + dst_off * V16;
+                        for (int i = lane; i < HT * V16; i += 32) {
+                            const uint4 k0 = ks[2 * i], k1 = ks[2 * i + 1];
+                            const uint4 v0 = vs[2 * i], v1 = vs[2 * i + 1];
+                            kd[i] = make_uint4(e4m3x4_of(k0.x, k0.y, a.k_scale_q), e4m3x4_of(k0.z, k0.w, a.k_scale_q),
+                                               e4m3x4_of(k1.x, k1.y, a.k_scale_q), e4m3x4_of(k1.z, k1.w, a.k_scale_q));
+                            vd[i] = make_uint4(e4m3x4_of(v0.x, v0.y, a.v_scale_q), e4m3x4_of(v0.z, v0.w, a.v_scale_q),
+                                               e4m3x4_of(v1.x, v1.y, a.v_scale_q), e4m3x4_of(v1.z, v1.w, a.v_scale_q));
+                        }
+                    } else {
+                        constexpr int V8 = D / 8;  // 16-byte vectors per head row
+                        const uint4 *ks = reinterpret_cast<const uint4 *>(a.k_new) + src_off * V8;
+                        const uint4 *vs = reinterpret_cast<const uint4 *>(a.v_new) + src_off * V8;
+                        uint4 *kd = reinterpret_cast<uint4 *>(a.k_cache_w) + dst_off * V8;
+                        uint4 *vd = reinterpret_cast<uint4 *>(a.v_cache_w) + dst_off * V8;
+                        for (int i = lane; i < HT * V8; i += 32) {
+                            kd[i] = ks[i];
+                            vd[i] = vs[i];
+                        }
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __syncwarp();
+                }
                 if (lane == 0) {
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {

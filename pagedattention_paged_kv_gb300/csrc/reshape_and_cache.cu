@@ -9,9 +9,8 @@
 // One warp per (token, K-or-V) row: the row (num_kv_heads * head_dim * 2 bytes,
 // 2 KiB for Llama-70B shapes) moves as 16-byte vectors, fully coalesced on both sides.
 // The source is read once (no L1 allocation); the destination is written normally.
-#include <cuda_fp8.h>
-
 #include "attn_block.cuh"
+#include "kv_quant.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
@@ -41,19 +40,8 @@ reshape_and_cache_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cach
     }
 }
 
-// FP8 cache: each element of a row is stored as the e4m3 code nearest to
-// fp32(x) / scale (IEEE division, round-to-nearest-even conversion saturating at
-// +-448).  One warp per (token, K-or-V) row; a lane turns 16 bf16 (32 bytes, two
-// 16-byte loads) into 16 codes (one 16-byte store).
-__device__ __forceinline__ uint32_t e4m3_of(uint32_t bf16_bits, float scale) {
-    const float y = __fdiv_rn(__uint_as_float(bf16_bits << 16), scale);
-    return (uint32_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ uint32_t e4m3x4_of(uint32_t w0, uint32_t w1, float scale) {
-    return e4m3_of(w0 & 0xFFFFu, scale) | (e4m3_of(w0 >> 16, scale) << 8) |
-           (e4m3_of(w1 & 0xFFFFu, scale) << 16) | (e4m3_of(w1 >> 16, scale) << 24);
-}
+// FP8 cache: one warp per (token, K-or-V) row; a lane turns 16 bf16 (32 bytes, two
+// 16-byte loads) into 16 codes (one 16-byte store) with e4m3x4_of (kv_quant.cuh).
 
 __global__ void __launch_bounds__(256)
 reshape_and_cache_fp8_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
