@@ -63,7 +63,8 @@ __device__ __forceinline__ void qk_block(float (&s)[2][4], const uint32_t (&qa)[
 // exceeds it by more than kRescaleSlack (log2 units): until then exp2(s - m) <= 2^8, so
 // neither the bf16 (or fp16) weights nor the fp32 sums can overflow, and most blocks
 // skip the rescale of O entirely.  The weights are rounded to bf16 (fp16) for the PV
-// MMA and l sums exactly those rounded weights.
+// MMA; with bf16 weights l sums exactly those rounded weights (so a one-token context
+// returns V exactly), with fp16 weights it sums the fp32 ones.
 constexpr float kRescaleSlack = 8.0f;
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -115,10 +116,12 @@ __device__ __forceinline__ void softmax_update(RowState<D> &st, float (&s)[2][4]
         const float e2 = fast_exp2(s[nt][2] - b1), e3 = fast_exp2(s[nt][3] - b1);
         uint32_t p01, p23;
         if constexpr (F16P) {
+            // fp16 keeps 11 significant bits: the sum adds the fp32 weights (their rounding
+            // moves l by at most 2^-12 relative) instead of widening the rounded ones again
             p01 = pack_f16x2(e0, e1);
             p23 = pack_f16x2(e2, e3);
-            ps0 += f16_lo(p01) + f16_hi(p01);
-            ps1 += f16_lo(p23) + f16_hi(p23);
+            ps0 += e0 + e1;
+            ps1 += e2 + e3;
         } else {
             p01 = pack_bf16x2(e0, e1);
             p23 = pack_bf16x2(e2, e3);

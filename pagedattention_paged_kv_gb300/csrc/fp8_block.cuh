@@ -76,35 +76,40 @@ __device__ __forceinline__ void load_q_fp8order(uint32_t (&qa)[8][4], const __nv
 }
 
 // S (16 rows x 16 tokens, fp32) = Q K^T (K in e4m3 codes; the K scale is applied to S
-// by the caller).  Four accumulator chains as in the bf16 version.
+// by the caller).  Eight accumulator chains of two MMAs each (k-steps ks and ks + 4 of one
+// n-tile share a chain): the legacy MMA's latency, not its issue rate, bounds this loop.
 __device__ __forceinline__ void qk_block_fp8(float (&s)[2][4], const uint32_t (&qa)[8][4], uint32_t tile, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float u[2][4];
+    float c[2][4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[0][i] = s[1][i] = u[0][i] = u[1][i] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[nt][k][i] = 0.f;
+    uint32_t w[2][8];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int tok = nt * 8 + g;
-        uint32_t w[8];
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "=r"(w[nt][0]), "=r"(w[nt][1]), "=r"(w[nt][2]), "=r"(w[nt][3])
                      : "r"(tile + tok * 128 + (((2 * t) ^ (tok & 7)) << 4)));
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                     : "=r"(w[nt][4]), "=r"(w[nt][5]), "=r"(w[nt][6]), "=r"(w[nt][7])
                      : "r"(tile + tok * 128 + (((2 * t + 1) ^ (tok & 7)) << 4)));
+    }
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;  // dims 32t + 4ks + {0, 1} and {2, 3}
-            e4m3x4_to_f16x2x2(w[ks], b0, b1);
-            if (ks & 1) mma_f16_16816(u[nt], qa[ks], b0, b1);
-            else mma_f16_16816(s[nt], qa[ks], b0, b1);
+            e4m3x4_to_f16x2x2(w[nt][ks], b0, b1);
+            mma_f16_16816(c[nt][ks & 3], qa[ks], b0, b1);
         }
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        s[0][i] += u[0][i];
-        s[1][i] += u[1][i];
-    }
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] = (c[nt][0][i] + c[nt][1][i]) + (c[nt][2][i] + c[nt][3][i]);
 }
 
 // O += P V for one block (V in e4m3 codes; the V scale is applied by the caller when the
