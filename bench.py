@@ -54,6 +54,8 @@ def parse():
                    help="tokens per pool block for the decode workloads (8, 16, 32, 64)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--graph-step", action="store_true",
+                   help="time the device step as a replayed CUDA graph of its launches")
     p.add_argument("--separate-kv-write", action="store_true",
                    help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
@@ -502,10 +504,22 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    cap_step = None
+    if args.graph_step:
+        from pagedattention_paged_kv_gb300.graph import CapturedStep
+        cap_step = CapturedStep(step)
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)              # evict the previous step's lines from L2
-            step(events[i])
+            if cap_step is None:
+                step(events[i])
+            else:
+                cap_step.stream.wait_stream(stream)
+                events[i][0].record(cap_step.stream)
+                events[i][1].record(cap_step.stream)
+                cap_step.replay()
+                events[i][2].record(cap_step.stream)
+                stream.wait_stream(cap_step.stream)
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
