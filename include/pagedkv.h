@@ -148,7 +148,7 @@ int pkv_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const
  * rounded to fp16 (exact for bf16 values of magnitude in [2^-14, 65504]), the
  * softmax weights are rounded to fp16.  Workspace as for the bf16 call
  * (pkv_workspace_size(PKV_OP_DECODE, ...)).
- * Supported: block_size 16, head_dim 128, the bf16 call's head counts.
+ * Supported: block_size 8, 16, 32 or 64, head_dim 128, the bf16 call's head counts.
  */
 int pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
                                    const void *v_cache, const int32_t *block_tables,
@@ -219,6 +219,30 @@ int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_st
                                int head_dim, int block_size, int64_t num_blocks, float scale,
                                int causal, int dtype, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * pkv_paged_attention_varlen_fp8: pkv_paged_attention_varlen over an FP8 cache (the
+ * encoding of pkv_reshape_and_cache_fp8): every cached K element reads as
+ * e4m3_value * k_scale and every V element as e4m3_value * v_scale; q and out stay
+ * bf16.  Single-token rows take the FP8 decode path (pkv_paged_attention_decode_fp8);
+ * multi-token rows run on the tensor cores in fp16 with fp32 accumulation: the codes
+ * widen to fp16 exactly, q is rounded to fp16, the softmax weights are rounded to fp16.
+ * Pool rows at or past a sequence's context are never read as values (they may hold
+ * any code, NaN included).  Workspace: pkv_workspace_size(PKV_OP_VARLEN, ...).
+ * Scales must be finite and > 0 (else PKV_ERR_INVALID_ARG).
+ * Supported: head_dim 128, block_size 16 when any row has q_len >= 2 (8, 16, 32 or 64
+ * otherwise), the bf16 call's head counts; PKV_ERR_UNSUPPORTED when a batch's
+ * per-sequence table and the kernel's stages do not fit in shared memory together
+ * (about 2,200 sequences in a batch with prefill rows).
+ */
+int pkv_paged_attention_varlen_fp8(void *out, const void *q, const int32_t *query_start_loc,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int total_q_tokens, int max_q_len,
+                                   int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks, float scale,
+                                   int causal, float k_scale, float v_scale, void *workspace,
+                                   size_t workspace_bytes, void *stream);
 
 /*
  * Decode attention that allocates nothing and takes no workspace.  The pages have no

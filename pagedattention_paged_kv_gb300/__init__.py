@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
                                                  i32, i64, f32, i32, vp, sz, vp]
         L.pkv_paged_attention_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                  i32, i32, i32, i32, i64, f32, i32, i32, vp, sz, vp]
+        L.pkv_paged_attention_varlen_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                     i32, i32, i32, i32, i64, f32, i32, f32, f32, vp, sz, vp]
         L.pkv_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, f32, f32, vp]
         L.pkv_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      i32, i64, f32, f32, f32, vp, sz, vp]
@@ -89,7 +91,7 @@ def lib() -> ctypes.CDLL:
         L.pkv_block_manager_num_free.restype = i64
         for name in ("pkv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_reshape_and_cache_fp8",
                      "pkv_paged_attention_decode_fp8",
-                     "pkv_paged_attention_varlen", "pkv_get_device_error", "pkv_slot_mapping",
+                     "pkv_paged_attention_varlen", "pkv_paged_attention_varlen_fp8", "pkv_get_device_error", "pkv_slot_mapping",
                      "pkv_block_manager_allocate", "pkv_block_manager_free", "pkv_copy_blocks",
                      "pkv_block_manager_share", "pkv_block_manager_ref_count",
                      "pkv_block_manager_copy_on_write", "pkv_paged_attention_decode_kvwrite",
@@ -237,15 +239,18 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_l
 
 def paged_attention_varlen(out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens,
                            scale: float, causal: bool = True, max_q_len: int | None = None,
-                           workspace=None, stream=None) -> None:
+                           workspace=None, stream=None, k_scale: float | None = None,
+                           v_scale: float | None = None) -> None:
     """out/q [total_q, Hq, d] bf16; query_start_loc [S+1] int32 (on the device);
-    max_q_len is the longest q_len (read back from the device if not given)."""
+    max_q_len is the longest q_len (read back from the device if not given).  A uint8
+    (e4m3) cache needs k_scale and v_scale; a bf16 cache takes none."""
     import torch
+    fp8 = k_cache.dtype == torch.uint8
     _require(out, torch.bfloat16, "out", 3)
     _require(q, torch.bfloat16, "q", 3)
     _require(query_start_loc, torch.int32, "query_start_loc", 1)
-    _require(k_cache, torch.bfloat16, "k_cache", 4)
-    _require(v_cache, torch.bfloat16, "v_cache", 4)
+    _require(k_cache, torch.uint8 if fp8 else torch.bfloat16, "k_cache", 4)
+    _require(v_cache, k_cache.dtype, "v_cache", 4)
     _require(block_tables, torch.int32, "block_tables", 2)
     _require(context_lens, torch.int32, "context_lens", 1)
     total_q, Hq, d = q.shape
@@ -254,15 +259,21 @@ def paged_attention_varlen(out, q, query_start_loc, k_cache, v_cache, block_tabl
     if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape \
             or block_tables.shape[0] != S or query_start_loc.shape[0] != S + 1:
         raise ValueError("shape mismatch")
+    if fp8 and (k_scale is None or v_scale is None):
+        raise ValueError("an FP8 cache needs k_scale and v_scale")
     if max_q_len is None:
         max_q_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
     nbytes = workspace_size(OP_VARLEN, S, total_q, Hq, Hkv, d, bs)
     ws = _workspace(workspace, nbytes, q.device)
-    _check(lib().pkv_paged_attention_varlen(
-        _ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
-        _ptr(block_tables), _ptr(context_lens), S, total_q, int(max_q_len), block_tables.shape[1],
-        Hq, Hkv, d, bs, NB, float(scale), int(bool(causal)), DTYPE_BF16, _ptr(ws),
-        ws.numel() * ws.element_size(), _stream_ptr(stream)), "paged_attention_varlen")
+    args = [_ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), S, total_q, int(max_q_len), block_tables.shape[1],
+            Hq, Hkv, d, bs, NB, float(scale), int(bool(causal))]
+    tail = [_ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)]
+    if fp8:
+        _check(lib().pkv_paged_attention_varlen_fp8(*args, float(k_scale), float(v_scale), *tail),
+               "paged_attention_varlen_fp8")
+    else:
+        _check(lib().pkv_paged_attention_varlen(*args, DTYPE_BF16, *tail), "paged_attention_varlen")
 
 
 def paged_attention_decode_kvwrite(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,

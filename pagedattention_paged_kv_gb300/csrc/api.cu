@@ -479,18 +479,22 @@ extern "C" int pkv_paged_attention_decode_kvwrite_fp8(void *out, const void *q, 
                           scale, true, k_scale, v_scale, workspace, workspace_bytes, stream);
 }
 
-extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
-                                          const void *k_cache, const void *v_cache,
-                                          const int32_t *block_tables,
-                                          const int32_t *context_lens, int num_seqs,
-                                          int total_q_tokens, int max_q_len,
-                                          int max_blocks_per_seq, int num_heads, int num_kv_heads,
-                                          int head_dim, int block_size, int64_t num_blocks,
-                                          float scale, int causal, int dtype, void *workspace,
-                                          size_t workspace_bytes, void *stream) {
+// Varlen batch (bf16 or FP8 cache): decode rows through the decode kernel, prefill
+// rows through the chunked-prefill kernel; see pagedkv.h.
+static int varlen(void *out, const void *q, const int32_t *query_start_loc, const void *k_cache,
+                  const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                  int num_seqs, int total_q_tokens, int max_q_len, int max_blocks_per_seq,
+                  int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                  float scale, int causal, int dtype, bool fp8, float k_scale, float v_scale,
+                  void *workspace, size_t workspace_bytes, void *stream) {
     int st = check_common(num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
                           block_size, num_blocks, dtype);
     if (st != PKV_OK) return st;
+    if (fp8) {
+        if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+        if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY)
+            return PKV_ERR_INVALID_ARG;
+    }
     if (total_q_tokens < 0 || max_q_len < 0) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
     if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -502,14 +506,14 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     st = device_info(&d);
     if (st != PKV_OK) return st;
     DecodePlan p;
-    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p);
+    st = plan_decode(num_seqs, num_heads, num_kv_heads, head_dim, *d, &p, fp8 ? 1 : 2);
     if (st != PKV_OK) return st;
     pkv::PrefillPlan pp;
     const bool prefill_rows = max_q_len >= 2;
     if (prefill_rows && block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
     if (prefill_rows) {
         st = pkv::plan_prefill(num_seqs, num_heads, num_kv_heads, head_dim, d->sms, d->smem_optin,
-                               &pp);
+                               &pp, fp8);
         if (st != PKV_OK) return st;
     }
     const size_t need = round_up(p.bytes, 256) + (prefill_rows ? pp.ws_bytes : 0);
@@ -519,16 +523,16 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     // Single-token rows: the decode kernel (it skips every other sequence).
     st = run_decode(out, q, query_start_loc, total_q_tokens, k_cache, v_cache, block_tables, context_lens,
                     num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
-                    scale, ws, p.bytes, *d, p, s, block_size);
+                    scale, ws, p.bytes, *d, p, s, block_size, fp8, k_scale, v_scale);
     if (st != PKV_OK || !prefill_rows) return st;
     // Multi-token rows (prefill chunks): the chunked-prefill kernel.
     CUtensorMap qmap, kmap, vmap;
     // one box per tile half
     st = encode_q_map(&qmap, q, total_q_tokens, num_heads, head_dim, pp.group, pp.tokens_per_tile / 2);
     if (st == PKV_OK)
-        st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
+        st = encode_cache_map(&kmap, k_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, fp8);
     if (st == PKV_OK)
-        st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1);
+        st = encode_cache_map(&vmap, v_cache, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, fp8);
     if (st != PKV_OK) return st;
     pkv::PrefillArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -545,17 +549,51 @@ extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_
     a.tokens_per_tile = pp.tokens_per_tile;
     a.grid = pp.grid;
     a.num_stages = pp.num_stages;
+    a.num_stages8 = pp.num_stages8;
     a.causal = causal != 0;
     a.num_blocks = num_blocks;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);  // FP8: K = code x k_scale
+    a.v_scale = fp8 ? v_scale : 1.f;
     uint8_t *pws = ws + round_up(p.bytes, 256);
     a.ws_jobs = reinterpret_cast<pkv::MergeJob *>(pws + pp.off_jobs);
     a.ws_ml = reinterpret_cast<float2 *>(pws + pp.off_ml);
     a.ws_o = reinterpret_cast<float *>(pws + pp.off_o);
     a.max_seqs = num_seqs;
     a.err = d->err;
-    return pkv::launch_paged_prefill(head_dim, qmap, kmap, vmap, a, pp, s) == cudaSuccess ? PKV_OK
-                                                                                   : PKV_ERR_CUDA;
+    return pkv::launch_paged_prefill(head_dim, fp8, qmap, kmap, vmap, a, pp, s) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
+                                          const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int total_q_tokens, int max_q_len,
+                                          int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int64_t num_blocks,
+                                          float scale, int causal, int dtype, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    return varlen(out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                  total_q_tokens, max_q_len, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                  block_size, num_blocks, scale, causal, dtype, false, 1.f, 1.f, workspace,
+                  workspace_bytes, stream);
+}
+
+extern "C" int pkv_paged_attention_varlen_fp8(void *out, const void *q, const int32_t *query_start_loc,
+                                              const void *k_cache, const void *v_cache,
+                                              const int32_t *block_tables,
+                                              const int32_t *context_lens, int num_seqs,
+                                              int total_q_tokens, int max_q_len,
+                                              int max_blocks_per_seq, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int64_t num_blocks, float scale, int causal,
+                                              float k_scale, float v_scale, void *workspace,
+                                              size_t workspace_bytes, void *stream) {
+    return varlen(out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                  total_q_tokens, max_q_len, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                  block_size, num_blocks, scale, causal, PKV_DTYPE_BF16, true, k_scale, v_scale,
+                  workspace, workspace_bytes, stream);
 }
 
 // ---- decode with the library's own scratch array (no workspace, no allocation) ----

@@ -29,6 +29,7 @@
 //  * Waits are bounded in time; no CTA waits on another CTA.
 #include "attn_block.cuh"
 #include "fp32x2.cuh"
+#include "fp8_block.cuh"
 #include "merge.cuh"
 #include "paged_prefill.cuh"
 #include "pkv_split.cuh"
@@ -264,27 +265,37 @@ __device__ __forceinline__ void segment_at(const PrefillArgs &a, const int64_t *
     sg.tile_tokens = (int)min64(a.tokens_per_tile, sg.u.t.q_len - sg.u.qt * a.tokens_per_tile);
 }
 
-template <int D>
+// FP8: the cache holds e4m3 codes (head_dim 128).  The producer loads them into a ring of
+// byte stages; warps 2 and 3 widen each chunk to fp16 into the operand ring the MMAs read
+// (same swizzled layout as the bf16 path), zero V rows past the context, and convert each
+// tile's Q to fp16 in place; the MMAs run kind::f16 with fp16 operands and P is fp16.
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
+    static_assert(!FP8 || D == 128, "the FP8 prefill is built for head_dim 128");
     using L = PrefillSmem<D>;
     constexpr int DCH = D / 64;
-    constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, L::KT, 0, 0);
-    constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, D, 0, 1);
+    constexpr uint32_t IDESC_QK = FP8 ? umma_idesc_f16(128, L::KT, 0, 0) : umma_idesc_bf16(128, L::KT, 0, 0);
+    constexpr uint32_t IDESC_PV = FP8 ? umma_idesc_f16(128, D, 0, 1) : umma_idesc_bf16(128, D, 0, 1);
+    constexpr uint32_t STG8 = L::KT * D;  // e4m3 K or V of one chunk
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = a.num_stages;
     uint8_t *sQ = smem, *sStage = smem + L::OFF_STAGES, *sEpi = smem + L::OFF_EPI;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + (size_t)NST * L::STG);
+    const int NST8 = FP8 ? a.num_stages8 : 0;
+    uint8_t *s8 = sStage + (size_t)NST * L::STG;  // FP8: the e4m3 staging ring
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s8 + (size_t)NST8 * STG8);
     // per half h: s_full[h], p_full[h], pv_done[h], o_free[h]
     uint64_t *q_full = bars, *q_empty = bars + 1, *mma_done = bars + 2;
     uint64_t *s_full = bars + 3, *p_full = bars + 5, *pv_done = bars + 7, *o_free = bars + 9;
     uint64_t *kv_full = bars + 11, *kv_empty = kv_full + NST;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(kv_empty + NST);
+    // FP8: e4m3 stages landed / converted; Q of the segment converted to fp16
+    uint64_t *f8_full = kv_empty + NST, *f8_empty = f8_full + NST8, *q_ready = f8_empty + NST8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int64_t *scan_tmp = reinterpret_cast<int64_t *>(tmem_slot + 2);  // 32 entries
     int64_t *pre = scan_tmp + 32;
@@ -304,9 +315,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_init(&o_free[h], 128);
         }
         for (int i = 0; i < NST; ++i) {
-            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_full[i], FP8 ? 64 : 1);  // FP8: the 64 converter threads arrive
             mbar_init(&kv_empty[i], 1);
         }
+        for (int i = 0; i < NST8; ++i) {
+            mbar_init(&f8_full[i], 1);
+            mbar_init(&f8_empty[i], 64);
+        }
+        mbar_init(q_ready, 64);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -382,20 +398,31 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                         for (int kv = 0; kv < 2; ++kv) {
                             const uint32_t st = pst;
-                            if (!mbar_wait(&kv_empty[st], pph ^ 1, abort_flag)) {
+                            // FP8: the e4m3 staging ring (the converters fill the operand ring)
+                            uint64_t *fb = FP8 ? &f8_full[st] : &kv_full[st];
+                            uint64_t *eb = FP8 ? &f8_empty[st] : &kv_empty[st];
+                            if (!mbar_wait(eb, pph ^ 1, abort_flag)) {
                                 ok = false;
                                 break;
                             }
-                            if (++pst == (uint32_t)NST) { pst = 0; pph ^= 1; }
-                            mbar_arrive_expect_tx(&kv_full[st], L::STG);
-                            uint8_t *dst = sStage + (size_t)st * L::STG;
+                            if (++pst == (uint32_t)(FP8 ? NST8 : NST)) { pst = 0; pph ^= 1; }
                             const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
+                            if constexpr (FP8) {
+                                mbar_arrive_expect_tx(fb, STG8);
+                                uint8_t *dst = s8 + (size_t)st * STG8;  // [key][128 bytes], 128-byte swizzle
 #pragma unroll
-                            for (int i = 0; i < L::BPC; ++i)
+                                for (int i = 0; i < L::BPC; ++i)
+                                    tma_load_5d(dst + i * (kBS * 128), map, fb, 0, 0, u.kvh, 0, ids[i], policy);
+                            } else {
+                                mbar_arrive_expect_tx(fb, L::STG);
+                                uint8_t *dst = sStage + (size_t)st * L::STG;
 #pragma unroll
-                                for (int dc = 0; dc < DCH; ++dc)
-                                    tma_load_5d(dst + dc * L::KV_DC + i * (kBS * 128), map, &kv_full[st],
-                                                0, 0, u.kvh, dc, ids[i], policy);
+                                for (int i = 0; i < L::BPC; ++i)
+#pragma unroll
+                                    for (int dc = 0; dc < DCH; ++dc)
+                                        tma_load_5d(dst + dc * L::KV_DC + i * (kBS * 128), map, fb, 0, 0,
+                                                    u.kvh, dc, ids[i], policy);
+                            }
                             ++fill;
                         }
                     }
@@ -409,9 +436,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             flag_error(a.err, PKV_DEVERR_TIMEOUT);
             *abort_flag = 1;
             // let issued copies land before shared memory is released
-            const uint32_t pending = minu32(fill, (uint32_t)NST);
+            const uint32_t nring = FP8 ? NST8 : NST;
+            const uint32_t pending = minu32(fill, nring);
             for (uint32_t k = fill - pending; k < fill; ++k)
-                mbar_wait(&kv_full[k % NST], (k / NST) & 1, nullptr);
+                mbar_wait(FP8 ? &f8_full[k % nring] : &kv_full[k % nring], (k / nring) & 1, nullptr);
             if (seg_i > 0) mbar_wait(q_full, (seg_i - 1) & 1, nullptr);
         }
     } else if (warp == 1) {
@@ -460,7 +488,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             segment_at<L::BPC>(a, pre, f, hi, sg);
             const int chunks = __shfl_sync(0xffffffffu, sg.chunks, 0);
             const int nh = __shfl_sync(0xffffffffu, sg.tile_tokens > HTOK ? 2 : 1, 0);  // halves with rows
-            if (!wait_all(q_full, seg_i & 1)) { ok = false; break; }
+            if (!wait_all(FP8 ? q_ready : q_full, seg_i & 1)) { ok = false; break; }
             // chunk 0's K and V slots
             uint32_t ks_ = kst, kp_ = kph;
             uint32_t vs_ = kst, vp_ = kph;
@@ -537,6 +565,74 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             mbar_wait(mma_done, 0, nullptr);
         }
         __syncwarp();
+    } else if (FP8 && (warp == 2 || warp == 3)) {
+        // ------------------ FP8: e4m3 -> fp16 converters (64 threads) ------------------
+        // They walk the same segments and chunks as the producer.  Per segment: once the
+        // tile's Q (bf16) has landed, convert it to fp16 in place and signal q_ready.  Per K or
+        // V chunk: wait for its e4m3 stage and a free operand slot, widen 128 keys x 128
+        // columns into the slot's layout ([64-column chunk][key][128 bytes], chunk c of a row
+        // at c ^ (key % 8)), zero V rows at or past the context (the pool may hold NaN codes
+        // there), then release the e4m3 stage and mark the slot full.  Generic stores become
+        // visible to the tensor core through fence.proxy.async before each arrive.
+        const int ctid = threadIdx.x - 64;
+        uint32_t s8i = 0, p8 = 0, s16 = 0, p16 = 0;
+        int seg_i = 0;
+        bool ok = true;
+        for (int64_t f = lo; f < hi && ok;) {
+            Segment sg;
+            segment_at<L::BPC>(a, pre, f, hi, sg);
+            if (!mbar_wait(q_full, seg_i & 1, abort_flag)) { ok = false; break; }
+            uint4 *q4 = reinterpret_cast<uint4 *>(sQ);
+            for (int i = ctid; i < (int)(L::Q_BYTES / 16); i += 64) {
+                uint4 x = q4[i];
+                x.x = bf16x2_to_f16x2(x.x);
+                x.y = bf16x2_to_f16x2(x.y);
+                x.z = bf16x2_to_f16x2(x.z);
+                x.w = bf16x2_to_f16x2(x.w);
+                q4[i] = x;
+            }
+            fence_async_smem();
+            mbar_arrive(q_ready);
+            const int ctx = sg.u.t.ctx;
+            for (int ch = 0; ch < sg.chunks && ok; ++ch) {
+                const int64_t key0 = (sg.u.kb + (int64_t)L::BPC * ch) * kBS;
+#pragma unroll 1
+                for (int kv = 0; kv < 2; ++kv) {
+                    if (!mbar_wait(&f8_full[s8i], p8, abort_flag) || !mbar_wait(&kv_empty[s16], p16 ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *src = s8 + (size_t)s8i * STG8;
+                    uint8_t *dst = sStage + (size_t)s16 * L::STG;
+                    const int zero_from = kv == 1 ? (int)max64(0, min64(ctx - key0, (int64_t)L::KT)) : L::KT;
+                    for (int i = ctid; i < L::KT * 8; i += 64) {
+                        const int key = i >> 3, c8 = i & 7;  // 16 codes = columns 16 c8 .. 16 c8 + 15
+                        const uint4 x = *reinterpret_cast<const uint4 *>(src + key * 128 + ((c8 ^ (key & 7)) << 4));
+                        uint4 lo4, hi4;
+                        e4m3x4_to_f16x2x2(x.x, lo4.x, lo4.y);
+                        e4m3x4_to_f16x2x2(x.y, lo4.z, lo4.w);
+                        e4m3x4_to_f16x2x2(x.z, hi4.x, hi4.y);
+                        e4m3x4_to_f16x2x2(x.w, hi4.z, hi4.w);
+                        if (key >= zero_from) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
+                        const int cp = (c8 & 3) * 2;  // first 16-byte chunk of the pair in a 64-column row
+                        uint8_t *row = dst + (c8 >> 2) * L::KV_DC + key * 128;
+                        *reinterpret_cast<uint4 *>(row + ((cp ^ (key & 7)) << 4)) = lo4;
+                        *reinterpret_cast<uint4 *>(row + (((cp + 1) ^ (key & 7)) << 4)) = hi4;
+                    }
+                    fence_async_smem();
+                    mbar_arrive(&kv_full[s16]);
+                    mbar_arrive(&f8_empty[s8i]);
+                    if (++s8i == (uint32_t)NST8) { s8i = 0; p8 ^= 1; }
+                    if (++s16 == (uint32_t)NST) { s16 = 0; p16 ^= 1; }
+                }
+            }
+            f = sg.end;
+            ++seg_i;
+        }
+        if (!ok) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
     } else if (warp >= 4) {
         // -------------- softmax: one warpgroup per half, one row per thread --------------
         const int h = (warp - 4) >> 2;
@@ -649,7 +745,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                             float x0, x1;
                             f2_unpack(x2, x0, x1);
                             const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-                            pk[j] = pack_bf16x2(e0, e1);
+                            pk[j] = FP8 ? pack_f16x2(e0, e1) : pack_bf16x2(e0, e1);
                             ps2[j & 1] = f2_add(ps2[j & 1], f2_pack(e0, e1));
                         }
                         tmem_st16(tS + (2 * r + q) * 16, pk);
@@ -662,7 +758,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                     l += (a0 + a1) + (b0 + b1);
                 }
                 tmem_wait_st();
-                if (h == 0 && key0 + nkeys > ctx) {
+                if (!FP8 && h == 0 && key0 + nkeys > ctx) {
                     // The chunk runs past the context: the pool rows there may hold NaN, and
                     // 0 * NaN would poison O, so zero those V rows before PV reads them (the
                     // second half's PV is issued after the first half's, so it sees them too).
@@ -686,7 +782,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             if (!mbar_wait(&pv_done[h], gl & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const bool whole = lo <= u.tile_begin && sg.end == u.tile_begin + u.tile_blocks;
-            const float inv = 1.f / l;
+            const float vsc = FP8 ? a.v_scale : 1.f;  // FP8: V elements are code x v_scale
+            const float inv = vsc / l;
             const int slot = whole ? 0 : part_slot(c, u.tile_begin, T, ge);
             const int trow = tok * group + hg;  // row inside the tile
             // Staged through this warp's 32 x 128-byte buffer: each lane writes its row's
@@ -745,6 +842,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                     tmem_ld32(tO + q * 32, v);
                     tmem_wait_ld();
                     reg_order32(v);
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * vsc);
+                    }
                     stage_and_store(v, [&](int hr) -> uint8_t * {
                         int tk, hgr;
                         if (!row_ok(hr, tk, hgr)) return nullptr;
@@ -773,8 +874,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
 // ---- host side -------------------------------------------------------------------
 
 int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
-                 int smem_optin, PrefillPlan *p) {
+                 int smem_optin, PrefillPlan *p, bool fp8) {
     if (num_kv_heads <= 0 || num_heads % num_kv_heads) return PKV_ERR_UNSUPPORTED;
+    if (fp8 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     p->group = num_heads / num_kv_heads;
     if (p->group > 8) return PKV_ERR_UNSUPPORTED;
     // A tile is two halves of 16 * (8 / group) tokens x group heads (<= 128 rows each).
@@ -784,13 +886,27 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     p->grid = sms < 256 ? sms : 256;  // the merge kernel holds <= 256 parts per tile
     p->max_seqs = num_seqs;
     const uint32_t q_bytes = (uint32_t)(head_dim / 64) * 2 * 128 * 128 + 8 * 4096;  // Q + epilogue staging
-    p->stage_bytes = 128 * head_dim * 2;  // K or V of a 128-key chunk
-    const size_t fixed = 1024 + q_bytes + 8 * 11 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
-    int nst = (int)(((int64_t)smem_optin - (int64_t)fixed) / (p->stage_bytes + 16));
-    if (nst > 8) nst = 8;
+    p->stage_bytes = 128 * head_dim * 2;  // K or V of a 128-key chunk (16-bit operands)
+    // barriers (11 + q_ready), TMEM slot and abort flag, scan scratch, per-sequence prefix
+    const size_t fixed = 1024 + q_bytes + 8 * 12 + 8 + 32 * 8 + 8 * (size_t)(num_seqs + 1);
+    const int64_t room = (int64_t)smem_optin - (int64_t)fixed;
+    int nst, nst8 = 0;
+    if (!fp8) {
+        nst = (int)(room / (p->stage_bytes + 16));
+        if (nst > 8) nst = 8;
+    } else {
+        // three fp16 operand slots (K of the next chunk loads while V of this one is read),
+        // then as many e4m3 stages (128 keys x 128 bytes) as fit, up to 4
+        nst = 3;
+        const int64_t stage8 = 128 * head_dim;
+        nst8 = (int)((room - 3 * (int64_t)(p->stage_bytes + 16)) / (stage8 + 16));
+        if (nst8 > 4) nst8 = 4;
+        if (nst8 < 1) return PKV_ERR_UNSUPPORTED;
+    }
     if (nst < 3) return PKV_ERR_UNSUPPORTED;
     p->num_stages = nst;
-    p->smem = fixed + (size_t)nst * (p->stage_bytes + 16);
+    p->num_stages8 = nst8;
+    p->smem = fixed + (size_t)nst * (p->stage_bytes + 16) + (size_t)nst8 * (128 * head_dim + 16);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     p->off_jobs = 0;
     p->off_ml = up(sizeof(MergeJob) * (size_t)p->grid);
@@ -799,26 +915,27 @@ int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, in
     return PKV_OK;
 }
 
-template <int D>
+template <int D, bool FP8>
 static cudaError_t launch_prefill_d(const CUtensorMap &q_map, const CUtensorMap &k_map,
                                     const CUtensorMap &v_map, const PrefillArgs &a,
                                     const PrefillPlan &p, cudaStream_t stream) {
-    // The register split is only safe when the launch pool covers it.
-    static int regs = -1;
-    if (regs < 0) {
-        cudaFuncAttributes fa;
-        cudaError_t e0 = cudaFuncGetAttributes(&fa, paged_prefill_kernel<D>);
-        if (e0 != cudaSuccess) return e0;
-        regs = fa.numRegs;
+    auto kernel = paged_prefill_kernel<D, FP8>;
+    if constexpr (kPrefillRegsLow != kPrefillRegsHigh) {
+        // The register split is only safe when the launch pool covers it.
+        static int regs = -1;
+        if (regs < 0) {
+            cudaFuncAttributes fa;
+            cudaError_t e0 = cudaFuncGetAttributes(&fa, kernel);
+            if (e0 != cudaSuccess) return e0;
+            regs = fa.numRegs;
+        }
+        if ((int64_t)regs * kPrefillThreads < 128 * kPrefillRegsLow + 256 * kPrefillRegsHigh)
+            return cudaErrorInvalidConfiguration;
     }
-    if ((int64_t)regs * kPrefillThreads < 128 * kPrefillRegsLow + 256 * kPrefillRegsHigh ||
-        p.warps * 32 != kPrefillThreads)
-        return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (p.warps * 32 != kPrefillThreads || (FP8 && a.num_stages8 < 1)) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(paged_prefill_kernel<D>, dim3(a.grid), dim3(p.warps * 32), p.smem, stream, q_map,
-                   k_map, v_map, a);
+    e = launch_pdl(kernel, dim3(a.grid), dim3(p.warps * 32), p.smem, stream, q_map, k_map, v_map, a);
     if (e != cudaSuccess) return e;
     MergeArgs m;
     m.jobs = a.ws_jobs;
@@ -830,11 +947,15 @@ static cudaError_t launch_prefill_d(const CUtensorMap &q_map, const CUtensorMap 
     return launch_merge<D>(m, a.grid, stream);
 }
 
-cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &q_map, const CUtensorMap &k_map,
+cudaError_t launch_paged_prefill(int head_dim, bool fp8, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                  const CUtensorMap &v_map, const PrefillArgs &a,
                                  const PrefillPlan &p, cudaStream_t stream) {
-    return head_dim == 128 ? launch_prefill_d<128>(q_map, k_map, v_map, a, p, stream)
-                           : launch_prefill_d<64>(q_map, k_map, v_map, a, p, stream);
+    if (fp8) {
+        if (head_dim != 128) return cudaErrorInvalidValue;
+        return launch_prefill_d<128, true>(q_map, k_map, v_map, a, p, stream);
+    }
+    return head_dim == 128 ? launch_prefill_d<128, false>(q_map, k_map, v_map, a, p, stream)
+                           : launch_prefill_d<64, false>(q_map, k_map, v_map, a, p, stream);
 }
 
 }  // namespace pkv

@@ -33,10 +33,15 @@ struct PrefillArgs {
     float *ws_o;             // [2 * grid][rows][head_dim]
     int max_seqs;
     int *err;
+    // FP8 cache (the FP8 kernel): e4m3 K/V land in a ring of num_stages8 byte stages and are
+    // widened to fp16 into the num_stages-slot operand ring; V elements mean code x v_scale
+    // (the K scale is folded into scale_log2).
+    int num_stages8;
+    float v_scale;
 };
 
 struct PrefillPlan {
-    int group, tokens_per_tile, rows, warps, grid, num_stages, stage_bytes, max_seqs;
+    int group, tokens_per_tile, rows, warps, grid, num_stages, stage_bytes, max_seqs, num_stages8;
     size_t smem;
     size_t off_jobs, off_ml, off_o, ws_bytes;
 };
@@ -44,8 +49,8 @@ struct PrefillPlan {
 // Fills *p for these sizes (num_seqs bounds the per-sequence table); PKV_OK or
 // PKV_ERR_UNSUPPORTED.
 int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
-                 int smem_optin, PrefillPlan *p);
-cudaError_t launch_paged_prefill(int head_dim, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                 int smem_optin, PrefillPlan *p, bool fp8 = false);
+cudaError_t launch_paged_prefill(int head_dim, bool fp8, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                  const CUtensorMap &v_map, const PrefillArgs &a,
                                  const PrefillPlan &p, cudaStream_t stream);
 

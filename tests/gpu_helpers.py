@@ -88,7 +88,7 @@ def torch_u8(a: np.ndarray, device="cuda"):
 
 def gpu_step_fp8(b: PagedBatch, workspace=None):
     """FP8 pool (b from workloads.to_fp8_pool): slot mapping, the quantising KV write
-    and decode through the library.  Returns (out fp64, k_cache codes, v_cache codes,
+    and attention (decode, or varlen when b has query_start_loc) through the library.  Returns (out fp64, k_cache codes, v_cache codes,
     device error flags)."""
     import torch
     ks, vs = b.meta["k_scale"], b.meta["v_scale"]
@@ -100,8 +100,13 @@ def gpu_step_fp8(b: PagedBatch, workspace=None):
     cl = torch.from_numpy(b.context_lens).cuda()
     out = torch.full_like(q, float("nan"))
     pkv.reshape_and_cache_fp8(kc, vc, k, v, sm, ks, vs)
-    assert b.query_start_loc is None, "the FP8 path is decode only"
-    pkv.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, b.scale, ks, vs, workspace=workspace)
+    if b.query_start_loc is None:
+        pkv.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, b.scale, ks, vs, workspace=workspace)
+    else:
+        qsl = torch.from_numpy(b.query_start_loc).cuda()
+        pkv.paged_attention_varlen(out, q, qsl, kc, vc, bt, cl, b.scale, causal=b.causal,
+                                   max_q_len=int(b.q_lens.max()), workspace=workspace,
+                                   k_scale=ks, v_scale=vs)
     err = pkv.get_device_error()
     return bf16_bits_to_f64(bf16_to_np(out)), kc.cpu().numpy(), vc.cpu().numpy(), err
 
@@ -114,5 +119,5 @@ def oracle_step_fp8(b: PagedBatch, row_mask=None):
     kc, vc = b.k_cache.copy(), b.v_cache.copy()
     orc.reshape_and_cache_fp8(kc, vc, b.k_new, b.v_new, slots, ks, vs)
     out = orc.paged_attention_fp8(b.q, kc, vc, ks, vs, b.block_tables, b.context_lens, b.scale,
-                                  row_mask=row_mask)
+                                  query_start_loc=b.query_start_loc, causal=b.causal, row_mask=row_mask)
     return out, kc, vc

@@ -1,6 +1,7 @@
 """GPU parity of the FP8 (e4m3) cache path through the C ABI against the fp64 oracle:
-the quantising KV write bit for bit over the whole pool, decode attention within
-|gpu - ref| <= 1e-2 + 2e-2 |ref| of attention over the dequantised pool."""
+the quantising KV write bit for bit over the whole pool, decode and varlen (chunked
+prefill + decode) attention within |gpu - ref| <= 1e-2 + 2e-2 |ref| of attention over
+the dequantised pool."""
 import numpy as np
 import pytest
 
@@ -133,3 +134,94 @@ def test_fp8_rejects_unsupported_and_bad_scales():
         with pytest.raises(pkv.PagedKVError) as e:
             pkv.paged_attention_decode_fp8(torch.empty_like(q), q, kc, kc, bt, cl, 0.1, ks, vs)
         assert e.value.status == -1
+
+
+# ---- varlen batches: FP8 prefill chunks next to FP8 decodes ---------------------------
+
+@pytest.mark.parametrize("q_lens,ctx", [
+    ([2, 1, 17, 1, 100], [2, 30, 17, 1, 500]),           # whole prompts and decodes
+    ([512, 1, 1, 33], [16896, 600, 1, 1000]),            # a chunk with a long prefix
+    ([16, 15, 48, 1], [16, 40, 1100, 2]),                # tile-aligned and ragged chunks
+    ([5, 300], [5, 300]),                                 # first chunks of prompts
+])
+def test_fp8_varlen_chunks_and_decodes(q_lens, ctx):
+    """Pool rows past every context hold the NaN code: the prefill's converters must zero
+    V there and the softmax mask K there."""
+    b = W.make_batch("varlen", context_lens=ctx, q_lens=q_lens, num_heads=64, num_kv_heads=8,
+                     head_dim=128, seed=sum(q_lens) + 3, varlen=True, pool_fill="nan")
+    _check_fp8(W.to_fp8_pool(b))
+
+
+def test_fp8_mixed_varlen_full_size_sampled_chunk_rows():
+    b = W.to_fp8_pool(W.mixed_varlen())
+    mask = np.zeros(b.q.shape[0], np.uint8)
+    mask[np.r_[0, 1, 2, 15, 16, 17, 31, 32, np.arange(47, 512, 37), 510, 511]] = 1
+    mask[np.r_[512:520, 600:608]] = 1  # decode rows
+    _check_fp8(b, row_mask=mask)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (56, 8), (16, 16), (64, 8), (32, 4)])
+def test_fp8_varlen_head_layouts(Hq, Hkv):
+    b = W.make_batch("varlen_heads", context_lens=[70, 3, 129, 260], q_lens=[37, 1, 129, 131],
+                     num_heads=Hq, num_kv_heads=Hkv, head_dim=128, seed=Hq * 7 + Hkv,
+                     varlen=True, pool_fill="nan")
+    _check_fp8(W.to_fp8_pool(b))
+
+
+def test_fp8_varlen_non_causal_and_scales_other_than_powers_of_two():
+    b = W.make_batch("noncausal", context_lens=[40, 9, 200, 700], q_lens=[12, 1, 64, 300],
+                     num_heads=16, num_kv_heads=4, head_dim=128, seed=27, varlen=True, causal=False,
+                     pool_fill="nan")
+    _check_fp8(W.to_fp8_pool(b, k_scale=0.0123, v_scale=0.0371))
+
+
+def test_fp8_long_prefix_splits_across_ctas():
+    """One 256-token chunk behind a 20000-token prefix: its tiles split across CTAs and
+    the parts (scaled by v_scale before the merge) are combined."""
+    b = W.make_batch("longprefix", context_lens=[20256, 3], q_lens=[256, 1], num_heads=64,
+                     num_kv_heads=8, head_dim=128, seed=77, varlen=True, pool_fill="nan")
+    _check_fp8(W.to_fp8_pool(b, k_scale=0.02, v_scale=0.05))
+
+
+def test_fp8_prefill_matches_bf16_prefill_on_dequantised_pool():
+    """With power-of-two scales the dequantised pool is exact in bf16: the FP8 and bf16
+    prefill kernels over it agree within the tolerance."""
+    import torch
+    b8 = W.to_fp8_pool(W.make_batch("cross", context_lens=[700, 5, 1500], q_lens=[200, 1, 333],
+                                    num_heads=64, num_kv_heads=8, head_dim=128, seed=43, varlen=True))
+    orc = oracle.load()
+    lut = np.array([orc.e4m3_decode(c) for c in range(256)], np.float64)
+    kb = W.bf16_bits((lut[b8.k_cache] * b8.meta["k_scale"]).astype(np.float32))
+    vb = W.bf16_bits((lut[b8.v_cache] * b8.meta["v_scale"]).astype(np.float32))
+    q = torch_bf16(b8.q)
+    qsl = torch.from_numpy(b8.query_start_loc).cuda()
+    bt = torch.from_numpy(b8.block_tables).cuda()
+    cl = torch.from_numpy(b8.context_lens).cuda()
+    o8 = torch.empty_like(q)
+    o16 = torch.empty_like(q)
+    pkv.paged_attention_varlen(o8, q, qsl, torch_u8(b8.k_cache), torch_u8(b8.v_cache), bt, cl, b8.scale,
+                               k_scale=b8.meta["k_scale"], v_scale=b8.meta["v_scale"])
+    pkv.paged_attention_varlen(o16, q, qsl, torch_bf16(kb), torch_bf16(vb), bt, cl, b8.scale)
+    assert pkv.get_device_error() == 0
+    compare(bf16_bits_to_f64(bf16_to_np(o8)), bf16_bits_to_f64(bf16_to_np(o16)))
+
+
+def test_fp8_varlen_rejects_bad_scales_and_head_dim():
+    import torch
+    q = torch.zeros(4, 8, 128, dtype=torch.bfloat16, device="cuda")
+    qsl = torch.tensor([0, 3, 4], dtype=torch.int32, device="cuda")
+    kc = torch.zeros(4, 16, 2, 128, dtype=torch.uint8, device="cuda")
+    bt = torch.zeros(2, 1, dtype=torch.int32, device="cuda")
+    cl = torch.tensor([3, 1], dtype=torch.int32, device="cuda")
+    for ks, vs in ((0.0, 1.0), (1.0, float("nan"))):
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.paged_attention_varlen(torch.empty_like(q), q, qsl, kc, kc, bt, cl, 0.1, k_scale=ks, v_scale=vs)
+        assert e.value.status == -1
+    with pytest.raises(ValueError):
+        pkv.paged_attention_varlen(torch.empty_like(q), q, qsl, kc, kc, bt, cl, 0.1)
+    q64 = torch.zeros(4, 8, 64, dtype=torch.bfloat16, device="cuda")
+    kc64 = torch.zeros(4, 16, 2, 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_attention_varlen(torch.empty_like(q64), q64, qsl, kc64, kc64, bt, cl, 0.1,
+                                   k_scale=1.0, v_scale=1.0)
+    assert e.value.status == -2
