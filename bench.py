@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--config", default="gqa_decode",
                    choices=["gqa_decode", "tiny_decode", "skewed_decode", "mixed_varlen", "cb_trace",
-                            "gqa_decode_fp8"])
+                            "gqa_decode_fp8", "mixed_varlen_fp8"])
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--block-size", type=int, default=16,
                    help="tokens per pool block for the decode workloads (8, 16, 32, 64)")
@@ -79,6 +79,11 @@ WORKLOADS = {
                      {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
                       "block_size": 16, "chunk": "512 tokens at positions 16384-16895",
                       "decodes": "127 x context uniform[500,2500]"}),
+    "mixed_varlen_fp8": ("mixed_varlen_512chunk_at_16384_plus_127_decodes_fp8_e4m3_kv", 4001,
+                         {"num_seqs": 128, "num_heads": 64, "num_kv_heads": 8, "head_dim": 128,
+                          "block_size": 16, "chunk": "512 tokens at positions 16384-16895",
+                          "decodes": "127 x context uniform[500,2500]", "kv_dtype": "fp8_e4m3",
+                          "k_scale": 2.0 ** -6, "v_scale": 2.0 ** -6}),
 }
 
 
@@ -93,6 +98,8 @@ def make_batch(config, seed, block_size=16):
             seed=seed, block_size=block_size)
     if config == "gqa_decode_fp8":
         return W.to_fp8_pool(W.gqa_decode(seed=seed))
+    if config == "mixed_varlen_fp8":
+        return W.to_fp8_pool(W.mixed_varlen(seed=seed))
     return {"gqa_decode": W.gqa_decode, "tiny_decode": W.tiny_decode,
             "skewed_decode": W.skewed_decode, "mixed_varlen": W.mixed_varlen}[config](seed=seed)
 
@@ -219,7 +226,7 @@ DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "fp8_
                   "pkv_split.cuh", "merge.cuh")
 
 
-PREFILL_SOURCES = ("paged_prefill.cu", "paged_prefill.cuh", "tcgen05.cuh", "fp32x2.cuh", "attn_block.cuh",
+PREFILL_SOURCES = ("paged_prefill.cu", "paged_prefill.cuh", "tcgen05.cuh", "fp32x2.cuh", "attn_block.cuh", "fp8_block.cuh",
                    "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
 
 
@@ -276,7 +283,8 @@ def oracle_step_time(b, seqs):
     if is_fp8(b):
         ks, vs = b.meta["k_scale"], b.meta["v_scale"]
         orc.reshape_and_cache_fp8(kc, vc, b.k_new, b.v_new, slots, ks, vs)
-        orc.paged_attention_fp8(b.q, kc, vc, ks, vs, b.block_tables, b.context_lens, b.scale, row_mask=mask)
+        orc.paged_attention_fp8(b.q, kc, vc, ks, vs, b.block_tables, b.context_lens, b.scale,
+                                query_start_loc=b.query_start_loc, causal=b.causal, row_mask=mask)
     else:
         orc.reshape_and_cache(kc, vc, b.k_new, b.v_new, slots)
         orc.paged_attention(b.q, kc, vc, b.block_tables, b.context_lens, b.scale,
@@ -464,8 +472,9 @@ def main():
 
     def attention(o=out, qq=q, qs=qsl, tables=bt, lens=cl):
         if varlen:
+            kw = {"k_scale": ks, "v_scale": vs} if fp8 else {}
             pkv.paged_attention_varlen(o, qq, qs, kc, vc, tables, lens, b.scale, causal=b.causal,
-                                       max_q_len=max_q_len, workspace=ws)
+                                       max_q_len=max_q_len, workspace=ws, **kw)
         elif fused:
             kw = {"k_scale": ks, "v_scale": vs} if fp8 else {}
             pkv.paged_attention_decode_kvwrite(o, qq, k_new, v_new, kc, vc, tables, lens, b.scale, workspace=ws, **kw)
@@ -652,6 +661,7 @@ def main():
 def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
     """Times the chunk rows alone and the decode rows alone (same pool, same call)."""
     res = {}
+    fp8 = is_fp8(b)
     ql = b.q_lens
     groups = {"chunk": np.nonzero(ql >= 2)[0], "decodes": np.nonzero(ql == 1)[0]}
     for key, seqs in groups.items():
@@ -666,10 +676,11 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
         ws = torch.empty(pkv.workspace_size(pkv.OP_VARLEN, len(seqs), qq.shape[0], b.num_heads,
                                             b.num_kv_heads, b.head_dim), dtype=torch.uint8, device=dev)
         mq = int(ql[seqs].max())
+        kw = {"k_scale": b.meta["k_scale"], "v_scale": b.meta["v_scale"]} if fp8 else {}
 
         def call():
             pkv.paged_attention_varlen(o, qq, qsl, kc, vc, tables, lens, b.scale, causal=b.causal,
-                                       max_q_len=mq, workspace=ws)
+                                       max_q_len=mq, workspace=ws, **kw)
         for _ in range(5):
             call()
         ts = []
@@ -687,14 +698,16 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
             tf = fl / (t * 1e-3) / 1e12
             res["chunk_us"] = t * 1e3
             res["chunk_tflops"] = tf
-            traffic = recorded_traffic("prefill", PREFILL_SOURCES, config)
+            traffic = recorded_traffic("prefill_fp8" if fp8 else "prefill", PREFILL_SOURCES, config)
             res["roofline"] = {"bound": "tensor", "kernel": "paged_prefill_kernel (+ merge, timed together)",
                                "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
-                               "peak_source": "measured bf16_tflops (burst cuBLAS)",
+                               "peak_source": "measured bf16_tflops (burst cuBLAS)" + (
+                                   " x 1: the fp16 MMAs of the FP8 cache run at the bf16 dense rate"
+                                   if fp8 else ""),
                                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                                "algorithmic_flops": fl}
         else:
-            byts = int(b.context_lens[seqs].astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * 4
+            byts = int(b.context_lens[seqs].astype(np.int64).sum()) * b.num_kv_heads * b.head_dim * (2 if fp8 else 4)
             res["decodes_us"] = t * 1e3
             res["decodes_gbs"] = byts / (t * 1e-3) / 1e9
     return res

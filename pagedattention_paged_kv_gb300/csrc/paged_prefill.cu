@@ -575,6 +575,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         // there), then release the e4m3 stage and mark the slot full.  Generic stores become
         // visible to the tensor core through fence.proxy.async before each arrive.
         const int ctid = threadIdx.x - 64;
+        const int c_key = ctid >> 3, c8 = ctid & 7, k7 = c_key & 7;
+        const int cp = (c8 & 3) * 2;  // first 16-byte chunk of the pair in a 64-column row
+        const uint32_t c_src = c_key * 128 + ((c8 ^ k7) << 4);
+        const uint32_t c_dst = (c8 >> 2) * L::KV_DC + c_key * 128 + ((cp ^ k7) << 4);
+        const int c_pair = (((cp + 1) ^ k7) - (cp ^ k7)) << 4;  // +-16: the pair's second chunk
         uint32_t s8i = 0, p8 = 0, s16 = 0, p16 = 0;
         int seg_i = 0;
         bool ok = true;
@@ -583,6 +588,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
             segment_at<L::BPC>(a, pre, f, hi, sg);
             if (!mbar_wait(q_full, seg_i & 1, abort_flag)) { ok = false; break; }
             uint4 *q4 = reinterpret_cast<uint4 *>(sQ);
+#pragma unroll 8
             for (int i = ctid; i < (int)(L::Q_BYTES / 16); i += 64) {
                 uint4 x = q4[i];
                 x.x = bf16x2_to_f16x2(x.x);
@@ -602,22 +608,27 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                         ok = false;
                         break;
                     }
-                    const uint8_t *src = s8 + (size_t)s8i * STG8;
-                    uint8_t *dst = sStage + (size_t)s16 * L::STG;
+                    // Thread t always handles 16-code group c8 = t % 8 of keys t / 8 + 8 j (j < 16):
+                    // key % 8 is fixed per thread, so the swizzled offsets are too, and the
+                    // 16 steps differ by 1 KiB.  All 16 loads are issued before the first store
+                    // (the compiler may not move a load above a store it cannot disambiguate),
+                    // so the loop is not a chain of shared-memory round trips.
+                    const uint8_t *src = s8 + (size_t)s8i * STG8 + c_src;
+                    uint8_t *dst = sStage + (size_t)s16 * L::STG + c_dst;
                     const int zero_from = kv == 1 ? (int)max64(0, min64(ctx - key0, (int64_t)L::KT)) : L::KT;
-                    for (int i = ctid; i < L::KT * 8; i += 64) {
-                        const int key = i >> 3, c8 = i & 7;  // 16 codes = columns 16 c8 .. 16 c8 + 15
-                        const uint4 x = *reinterpret_cast<const uint4 *>(src + key * 128 + ((c8 ^ (key & 7)) << 4));
+                    uint4 x[L::KT / 8];
+#pragma unroll
+                    for (int j = 0; j < L::KT / 8; ++j) x[j] = *reinterpret_cast<const uint4 *>(src + j * 1024);
+#pragma unroll
+                    for (int j = 0; j < L::KT / 8; ++j) {
                         uint4 lo4, hi4;
-                        e4m3x4_to_f16x2x2(x.x, lo4.x, lo4.y);
-                        e4m3x4_to_f16x2x2(x.y, lo4.z, lo4.w);
-                        e4m3x4_to_f16x2x2(x.z, hi4.x, hi4.y);
-                        e4m3x4_to_f16x2x2(x.w, hi4.z, hi4.w);
-                        if (key >= zero_from) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
-                        const int cp = (c8 & 3) * 2;  // first 16-byte chunk of the pair in a 64-column row
-                        uint8_t *row = dst + (c8 >> 2) * L::KV_DC + key * 128;
-                        *reinterpret_cast<uint4 *>(row + ((cp ^ (key & 7)) << 4)) = lo4;
-                        *reinterpret_cast<uint4 *>(row + (((cp + 1) ^ (key & 7)) << 4)) = hi4;
+                        e4m3x4_to_f16x2x2(x[j].x, lo4.x, lo4.y);
+                        e4m3x4_to_f16x2x2(x[j].y, lo4.z, lo4.w);
+                        e4m3x4_to_f16x2x2(x[j].z, hi4.x, hi4.y);
+                        e4m3x4_to_f16x2x2(x[j].w, hi4.z, hi4.w);
+                        if (c_key + 8 * j >= zero_from) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(dst + j * 1024) = lo4;
+                        *reinterpret_cast<uint4 *>(dst + j * 1024 + c_pair) = hi4;
                     }
                     fence_async_smem();
                     mbar_arrive(&kv_full[s16]);
