@@ -575,7 +575,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
         // there), then release the e4m3 stage and mark the slot full.  Generic stores become
         // visible to the tensor core through fence.proxy.async before each arrive.
         const int ctid = threadIdx.x - 64;
-        const int c_key = ctid >> 3, c8 = ctid & 7, k7 = c_key & 7;
+        // Lanes 8q .. 8q+7 (one 128-byte phase of a 16-byte access) take 8 keys of the same
+        // 16-code group: their loads (chunk c8 ^ key % 8) and stores (chunk 2 (c8 % 4) ^ key % 8,
+        // and its pair) then hit 8 different bank groups.
+        const int c_key = ctid & 7, c8 = ctid >> 3, k7 = c_key;
         const int cp = (c8 & 3) * 2;  // first 16-byte chunk of the pair in a 64-column row
         const uint32_t c_src = c_key * 128 + ((c8 ^ k7) << 4);
         const uint32_t c_dst = (c8 >> 2) * L::KV_DC + c_key * 128 + ((cp ^ k7) << 4);
@@ -608,7 +611,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                         ok = false;
                         break;
                     }
-                    // Thread t always handles 16-code group c8 = t % 8 of keys t / 8 + 8 j (j < 16):
+                    // Thread t always handles 16-code group c8 = t / 8 of keys t % 8 + 8 j (j < 16):
                     // key % 8 is fixed per thread, so the swizzled offsets are too, and the
                     // 16 steps differ by 1 KiB.  All 16 loads are issued before the first store
                     // (the compiler may not move a load above a store it cannot disambiguate),
