@@ -9,7 +9,10 @@ the step's new tokens (host), the KV write (reshape_and_cache) and decode attent
 
 Prints ONE JSON line (rank 0).  `value` is HBM GB/s over the step's algorithmic bytes
 (every context K/V row once, queries, outputs, new rows, block-table entries) with
-inputs resident in HBM, timed with CUDA events per step and L2 flushed between steps;
+inputs resident in HBM and larger than L2, timed with CUDA events per step and L2
+flushed between steps by reading a 256 MB buffer (so the step starts with an L2 that
+holds none of its data and no dirty lines of the flush to write back; `--flush write`
+writes the buffer instead);
 `e2e` is the same metric with the step's inputs copied from pinned host memory (one
 packed copy) and the output copied back inside the timed region.  `--impl reference`
 times the fp64 CPU oracle on the same workload instead.  `--config` selects one of
@@ -56,6 +59,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--graph-step", action="store_true",
                    help="time the device step as a replayed CUDA graph of its launches")
+    p.add_argument("--flush", choices=["read", "write", "none"], default="read",
+                   help="between timed steps: read a 256 MB buffer (evicts the previous step's lines and "
+                        "leaves L2 clean), write one (evicts them but leaves ~126 MB of dirty lines that "
+                        "the step itself then writes back), or nothing (the inputs are larger than L2)")
     p.add_argument("--separate-kv-write", action="store_true",
                    help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
@@ -468,6 +475,14 @@ def main():
     op = pkv.OP_VARLEN if varlen else pkv.OP_DECODE
     ws = torch.empty(pkv.workspace_size(op, S, T, Hq, b.num_kv_heads, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def l2_flush(i):
+        if args.flush == "write":
+            flush.fill_(i & 0xFF)              # evict the previous step's lines from L2 (leaves them dirty)
+        elif args.flush == "read":
+            torch.sum(flush_rd, dim=0, out=flush_sink)  # evict them, leaving clean lines
     stream = torch.cuda.current_stream()
 
     def attention(o=out, qq=q, qs=qsl, tables=bt, lens=cl):
@@ -519,7 +534,7 @@ def main():
         cap_step = CapturedStep(step)
     with ClockSampler(local) as clk:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)              # evict the previous step's lines from L2
+            l2_flush(i)
             if cap_step is None:
                 step(events[i])
             else:
@@ -581,7 +596,7 @@ def main():
             n = min(args.steps, 500)
             times = []
             for i in range(n):
-                flush.fill_(i & 0xFF)
+                l2_flush(i)
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
                 step_fn()
@@ -609,7 +624,7 @@ def main():
     # ---- varlen only: the chunk alone and the decodes alone ----
     parts = None
     if varlen:
-        parts = varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, args.config)
+        parts = varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, args.config)
 
     if rank != 0:
         return
@@ -625,7 +640,10 @@ def main():
                    "slot_waste": slot_waste(b),
                    "sum_context": int(b.context_lens.astype(np.int64).sum()), "num_blocks": b.num_blocks,
                    "parallelism": f"replicas x{world}",
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write); KV pool "
+                   "l2": "inputs larger than L2 (126 MB) and " + {
+                       "write": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                       "read": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB read: clean eviction)",
+                       "none": "not flushed"}[args.flush] + "; KV pool "
                          f"2 x {b.k_cache.nbytes / 1e6:.0f} MB"},
         "pct_of_peak": 100.0 * value / world / hbm_peak,
         "seq_steps_per_s": S * world / (t_step * 1e-3),
@@ -658,7 +676,7 @@ def main():
     print(json.dumps(line), flush=True)
 
 
-def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
+def varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, config):
     """Times the chunk rows alone and the decode rows alone (same pool, same call)."""
     res = {}
     fp8 = is_fp8(b)
@@ -685,7 +703,7 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, flush, hbm_peak, tc_peak, config):
             call()
         ts = []
         for i in range(50):
-            flush.fill_(i & 0xFF)
+            l2_flush(i)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             call()
