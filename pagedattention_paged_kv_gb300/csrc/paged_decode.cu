@@ -155,8 +155,9 @@ __device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pr
     }
 }
 
-// FP8: the cache holds e4m3 codes (head_dim 128 only); see fp8_block.cuh.
-template <int D, bool FP8>
+// FP8: the cache holds e4m3 codes (head_dim 128 only); see fp8_block.cuh.  NTH: n-tiles of
+// query heads per consumer warp in the FP8 form (1: a KV head has at most 8 query heads).
+template <int D, bool FP8, int NTH>
 __global__ void __launch_bounds__(288, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
@@ -358,7 +359,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
     uint32_t stage = 0, phase = 0;
     int64_t f = lo;
-    RowState<D> st;
+    RowState<D> st;  // bf16 cache: heads on the MMA's M
+    HeadState<NTH> hs;  // FP8 cache: heads on the MMA's N (fp8_block.cuh)
     while (f < hi) {
         const int v = find_item(pre, V, f);
         const int s = v / a.head_tiles;
@@ -387,7 +389,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                 qa[ks][3] = v1 ? __ldg(q0 + ((g_row + 8) * D + col + 8) / 2) : 0u;
             }
         }
-        st.reset();
+        if constexpr (FP8) hs.reset();
+        else st.reset();
 
         bool ok = true;
         for (; f < seg_end; ++f) {
@@ -396,7 +399,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             // ---- S = Q K^T over the block's 16 tokens ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
             float sacc[2][4];
-            if constexpr (FP8) qk_block_fp8(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), lane);
+            if constexpr (FP8)
+                qk_block_fp8t<NTH>(reinterpret_cast<float(&)[NTH][4]>(sacc), qa,
+                                   smem_base + stage * stage_bytes + hh * (kBS * 128), lane);
             else qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
@@ -404,6 +409,28 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
             // ---- scale, mask the block's tail, online softmax (base 2) ----
             const bool tail = valid < kBS;  // only a sequence's last block
+            if constexpr (FP8) {
+                // S^T: tokens g (entries 0, 1) and g + 8 (entries 2, 3) of each n-tile
+                const bool in0 = !tail || g_row < valid, in1 = !tail || g_row + 8 < valid;
+                uint32_t pb[NTH][2];
+#pragma unroll
+                for (int nt = 0; nt < NTH; ++nt) {
+                    sacc[nt][0] = in0 ? sacc[nt][0] * sl2 : -INFINITY;
+                    sacc[nt][1] = in0 ? sacc[nt][1] * sl2 : -INFINITY;
+                    sacc[nt][2] = in1 ? sacc[nt][2] * sl2 : -INFINITY;
+                    sacc[nt][3] = in1 ? sacc[nt][3] * sl2 : -INFINITY;
+                    softmax_update_t(hs, nt, sacc[nt], pb[nt]);
+                }
+                // ---- O^T += V^T P^T ----
+                if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
+                if (tail) pv_block_fp8t<true>(hs, pb, vtile, valid, lane);
+                else pv_block_fp8t<false>(hs, pb, vtile, valid, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
+                continue;
+            }
             if (tail) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -421,18 +448,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                 }
             }
             uint32_t pa[4];
-            softmax_update<D, FP8>(st, sacc, pa);
+            softmax_update<D>(st, sacc, pa);
 
             // ---- O += P V ----
             if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
             const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-            if constexpr (FP8) {
-                if (tail) pv_block_fp8<true>(st.o, pa, vtile, valid, lane);
-                else pv_block_fp8<false>(st.o, pa, vtile, valid, lane);
-            } else {
-                if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
-                else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
-            }
+            if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
+            else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
@@ -444,58 +466,48 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         }
 
         // ---- finish this item's part ----
-        finish_sums<D>(st);
         const int64_t seg_beg = max64(lo, item_beg);
         const bool whole = seg_beg == item_beg && seg_end == item_end;
         if constexpr (FP8) {
-            // accumulators hold dims 32t + j (columns 0, 2) and 32t + 16 + j (1, 3); the
-            // V scale comes in here
+            // lane (g, t) holds dims 16g .. 16g + 15 of heads 8nt + 2t + e: dim 16g + 2mt in
+            // o[nt][mt][e], 16g + 2mt + 1 in o[nt][mt][2 + e]; the V scale comes in here
+            finish_sums_t(hs);
             const float vs = a.v_scale;
-            const bool w0 = g_row < rows_valid, w1 = g_row + 8 < rows_valid;
-            if (whole) {
-                const float inv0 = vs / st.l0, inv1 = vs / st.l1;
-                __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D + 32 * q4;
+            const int rows = HT * group;
+            const int row0 = hh * group + r0;  // row inside the item
+            const int slot = whole ? 0 : part_slot(c, item_beg, T, ge);
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
+            for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        uint4 x0, x1;
-                        uint32_t *p0 = &x0.x, *p1 = &x1.x;
+                for (int e = 0; e < 2; ++e) {
+                    const int hd = 8 * nt + 2 * q4 + e;  // head inside the warp's 16
+                    if (hd >= rows_valid) continue;
+                    if (whole) {
+                        const float inv = vs / hs.l[nt][e];
+                        uint32_t p[8];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int j = 8 * i + 2 * k;
-                            p0[k] = pack_bf16x2(st.o[j][half] * inv0, st.o[j + 1][half] * inv0);
-                            p1[k] = pack_bf16x2(st.o[j][2 + half] * inv1, st.o[j + 1][2 + half] * inv1);
-                        }
-                        if (w0) *reinterpret_cast<uint4 *>(orow + g_row * D + 16 * half + 8 * i) = x0;
-                        if (w1) *reinterpret_cast<uint4 *>(orow + (g_row + 8) * D + 16 * half + 8 * i) = x1;
+                        for (int mt = 0; mt < 8; ++mt)
+                            p[mt] = pack_bf16x2(hs.o[nt][mt][e] * inv, hs.o[nt][mt][2 + e] * inv);
+                        uint4 *orow = reinterpret_cast<uint4 *>(
+                            a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0 + hd) * D + 16 * g_row);
+                        orow[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                        orow[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    } else {
+                        float4 *ob = reinterpret_cast<float4 *>(a.ws_o + ((int64_t)slot * rows + row0 + hd) * D +
+                                                                16 * g_row);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ob[k] = make_float4(hs.o[nt][2 * k][e] * vs, hs.o[nt][2 * k][2 + e] * vs,
+                                                hs.o[nt][2 * k + 1][e] * vs, hs.o[nt][2 * k + 1][2 + e] * vs);
+                        if (g_row == 0)
+                            a.ws_ml[(int64_t)slot * rows + row0 + hd] = make_float2(hs.m[nt][e], hs.l[nt][e]);
                     }
-            } else {
-                const int slot = part_slot(c, item_beg, T, ge);
-                const int rows = HT * group;
-                const int row0 = hh * group + r0;  // row inside the item
-                float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D + 32 * q4;
-                float2 *mlb = a.ws_ml + (int64_t)slot * rows + row0;
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = 4 * i;
-                        if (w0)
-                            *reinterpret_cast<float4 *>(ob + g_row * D + 16 * half + j) =
-                                make_float4(st.o[j][half] * vs, st.o[j + 1][half] * vs,
-                                            st.o[j + 2][half] * vs, st.o[j + 3][half] * vs);
-                        if (w1)
-                            *reinterpret_cast<float4 *>(ob + (g_row + 8) * D + 16 * half + j) =
-                                make_float4(st.o[j][2 + half] * vs, st.o[j + 1][2 + half] * vs,
-                                            st.o[j + 2][2 + half] * vs, st.o[j + 3][2 + half] * vs);
-                    }
-                if (q4 == 0) {
-                    if (w0) mlb[g_row] = make_float2(st.m0, st.l0);
-                    if (w1) mlb[g_row + 8] = make_float2(st.m1, st.l1);
                 }
-            }
-        } else if (whole) {
+            f = seg_end;
+            continue;
+        }
+        finish_sums<D>(st);
+        if (whole) {
             const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
             __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
 #pragma unroll
@@ -531,11 +543,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     }
 }
 
-template __global__ void paged_decode_kernel<64, false>(const __grid_constant__ CUtensorMap,
+template __global__ void paged_decode_kernel<64, false, 1>(const __grid_constant__ CUtensorMap,
                                                         const __grid_constant__ CUtensorMap, const DecodeArgs);
-template __global__ void paged_decode_kernel<128, false>(const __grid_constant__ CUtensorMap,
+template __global__ void paged_decode_kernel<128, false, 1>(const __grid_constant__ CUtensorMap,
                                                          const __grid_constant__ CUtensorMap, const DecodeArgs);
-template __global__ void paged_decode_kernel<128, true>(const __grid_constant__ CUtensorMap,
+template __global__ void paged_decode_kernel<128, true, 1>(const __grid_constant__ CUtensorMap,
+                                                           const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<128, true, 2>(const __grid_constant__ CUtensorMap,
                                                         const __grid_constant__ CUtensorMap, const DecodeArgs);
 
 // ---- host-side launch ----------------------------------------------------------
@@ -545,14 +559,14 @@ size_t decode_smem_bytes(int stage_bytes, int num_stages, int num_items) {
            4 * (size_t)(num_items + 1);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NTH>
 static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
                                    const DecodeArgs &a, size_t smem, cudaStream_t stream) {
     const int ncw = a.heads_per_cta * a.warps_per_head;
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, FP8>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, FP8, NTH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(paged_decode_kernel<D, FP8>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
+    e = launch_pdl(paged_decode_kernel<D, FP8, NTH>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
                    v_map, a);
     if (e != cudaSuccess) return e;
     MergeArgs m;
@@ -567,10 +581,11 @@ static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &
 
 cudaError_t launch_paged_decode(int head_dim, bool fp8, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                 const DecodeArgs &a, size_t smem, cudaStream_t stream) {
-    if (fp8) return head_dim == 128 ? launch_decode_d<128, true>(k_map, v_map, a, smem, stream)
-                                    : cudaErrorInvalidValue;
-    return head_dim == 128 ? launch_decode_d<128, false>(k_map, v_map, a, smem, stream)
-                           : launch_decode_d<64, false>(k_map, v_map, a, smem, stream);
+    if (fp8 && head_dim != 128) return cudaErrorInvalidValue;
+    if (fp8) return a.group <= 8 ? launch_decode_d<128, true, 1>(k_map, v_map, a, smem, stream)
+                                 : launch_decode_d<128, true, 2>(k_map, v_map, a, smem, stream);
+    return head_dim == 128 ? launch_decode_d<128, false, 1>(k_map, v_map, a, smem, stream)
+                           : launch_decode_d<64, false, 1>(k_map, v_map, a, smem, stream);
 }
 
 }  // namespace pkv
