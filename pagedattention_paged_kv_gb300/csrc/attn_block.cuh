@@ -62,9 +62,9 @@ __device__ __forceinline__ void qk_block(float (&s)[2][4], const uint32_t (&qa)[
 // and set to -inf where masked.  The reference max moves only when a row's block max
 // exceeds it by more than kRescaleSlack (log2 units): until then exp2(s - m) <= 2^8, so
 // neither the bf16 (or fp16) weights nor the fp32 sums can overflow, and most blocks
-// skip the rescale of O entirely.  The weights are rounded to bf16 (fp16) for the PV
-// MMA; with bf16 weights l sums exactly those rounded weights (so a one-token context
-// returns V exactly), with fp16 weights it sums the fp32 ones.
+// skip the rescale of O entirely.  The weights are rounded to bf16 for the PV MMA and l
+// sums exactly those rounded weights (so a one-token context returns V exactly).  The
+// FP8 decode form (fp8_block.cuh) and the prefill kernel use the same rule.
 constexpr float kRescaleSlack = 8.0f;
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -78,8 +78,7 @@ __device__ __forceinline__ float f16_hi(uint32_t v) {
     return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
 
-// F16P: the weights are rounded to fp16 (for an fp16 PV MMA) instead of bf16.
-template <int D, bool F16P = false>
+template <int D>
 __device__ __forceinline__ void softmax_update(RowState<D> &st, float (&s)[2][4], uint32_t (&pa)[4]) {
     float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
     float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
@@ -114,20 +113,9 @@ __device__ __forceinline__ void softmax_update(RowState<D> &st, float (&s)[2][4]
     for (int nt = 0; nt < 2; ++nt) {
         const float e0 = fast_exp2(s[nt][0] - b0), e1 = fast_exp2(s[nt][1] - b0);
         const float e2 = fast_exp2(s[nt][2] - b1), e3 = fast_exp2(s[nt][3] - b1);
-        uint32_t p01, p23;
-        if constexpr (F16P) {
-            // fp16 keeps 11 significant bits: the sum adds the fp32 weights (their rounding
-            // moves l by at most 2^-12 relative) instead of widening the rounded ones again
-            p01 = pack_f16x2(e0, e1);
-            p23 = pack_f16x2(e2, e3);
-            ps0 += e0 + e1;
-            ps1 += e2 + e3;
-        } else {
-            p01 = pack_bf16x2(e0, e1);
-            p23 = pack_bf16x2(e2, e3);
-            ps0 += bf16_lo(p01) + bf16_hi(p01);
-            ps1 += bf16_lo(p23) + bf16_hi(p23);
-        }
+        const uint32_t p01 = pack_bf16x2(e0, e1), p23 = pack_bf16x2(e2, e3);
+        ps0 += bf16_lo(p01) + bf16_hi(p01);
+        ps1 += bf16_lo(p23) + bf16_hi(p23);
         pa[nt * 2 + 0] = p01;
         pa[nt * 2 + 1] = p23;
     }
