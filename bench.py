@@ -63,6 +63,9 @@ def parse():
                    help="between timed steps: read a 256 MB buffer (evicts the previous step's lines and "
                         "leaves L2 clean), write one (evicts them but leaves ~126 MB of dirty lines that "
                         "the step itself then writes back), or nothing (the inputs are larger than L2)")
+    p.add_argument("--e2e-copy", choices=["sm", "engine"], default="sm",
+                   help="e2e host<->device transfers: the library's SM copies (pkv.copy_to_device / "
+                        "copy_to_host, pinned host memory read and written by the SMs) or torch's copy-engine copies")
     p.add_argument("--separate-kv-write", action="store_true",
                    help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
@@ -562,10 +565,16 @@ def main():
         h_slots = io.host_view("slots")
 
         def device_part():
-            io.dev.copy_(io.host, non_blocking=True)
+            if args.e2e_copy == "sm":
+                pkv.copy_to_device(io.dev, io.host)
+            else:
+                io.dev.copy_(io.host, non_blocking=True)
             kv_write()
             attention()
-            hout.copy_(out, non_blocking=True)
+            if args.e2e_copy == "sm":
+                pkv.copy_to_host(hout, out)
+            else:
+                hout.copy_(out, non_blocking=True)
 
         def host_slots():
             # the fused decode step derives the new token's slot on the device
@@ -617,6 +626,8 @@ def main():
                "h2d_bytes_per_step": io.nbytes, "d2h_bytes_per_step": hout.numel() * 2,
                "ms_per_step": t_e2e * 1e3, "steps": n_e2e,
                "launch": "cuda_graph (pagedattention_paged_kv_gb300.graph.CapturedStep)" if t_graph else "eager",
+               "copies": "SM copy kernels over pinned host memory (pkv.copy_to_device / copy_to_host)"
+                         if args.e2e_copy == "sm" else "copy engines (torch Tensor.copy_)",
                "eager_ms_per_step": t_eager * 1e3}
         if graph_note:
             e2e["note"] = graph_note

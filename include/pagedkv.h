@@ -272,6 +272,23 @@ int pkv_paged_attention_decode_static(void *out, const void *q, const void *k_ca
                                       int head_dim, int block_size, int64_t num_blocks,
                                       float scale, int dtype, void *stream);
 
+/*
+ * Step transfers: copies `bytes` bytes from host src to device dst (pkv_copy_to_device)
+ * or from device src to host dst (pkv_copy_to_host), asynchronously on `stream`, in
+ * stream order with the library's kernels.  When the host buffer is page-locked and
+ * mapped into the device's address space (cudaHostAlloc, or cudaHostRegister with
+ * mapping, on a unified-addressing system), the copy runs as a kernel whose threads load
+ * or store the host memory directly (on GB300, over NVLink-C2C; for the few MB of a decode
+ * step this is several times faster than a copy-engine transfer); otherwise it is a
+ * cudaMemcpyAsync.  The device side must be memory of the current device
+ * (PKV_ERR_INVALID_ARG otherwise).  Ownership stays with the caller; for a page-locked
+ * host source the caller must not modify it until the copy has run.  Any alignment.
+ * Not from the pages: the end-to-end step they describe moves its inputs and outputs
+ * between host and device around the attention call.
+ */
+int pkv_copy_to_device(void *dst, const void *src, size_t bytes, void *stream);
+int pkv_copy_to_host(void *dst, const void *src, size_t bytes, void *stream);
+
 /* Workspace bytes the op needs on the current device for these sizes (0 if the
  * sizes are unsupported).  Does not allocate. */
 size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_block_manager_share.argtypes = [vp, vp, i64]
         L.pkv_block_manager_ref_count.argtypes = [vp, ctypes.c_int32]
         L.pkv_block_manager_copy_on_write.argtypes = [vp, ctypes.c_int32, vp]
+        L.pkv_copy_to_device.argtypes = [vp, vp, sz, vp]
+        L.pkv_copy_to_host.argtypes = [vp, vp, sz, vp]
         L.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.pkv_workspace_size.restype = sz
         L.pkv_status_string.argtypes = [i32]
@@ -95,7 +97,7 @@ def lib() -> ctypes.CDLL:
                      "pkv_block_manager_allocate", "pkv_block_manager_free", "pkv_copy_blocks",
                      "pkv_block_manager_share", "pkv_block_manager_ref_count",
                      "pkv_block_manager_copy_on_write", "pkv_paged_attention_decode_kvwrite",
-                     "pkv_paged_attention_decode_kvwrite_fp8"):
+                     "pkv_paged_attention_decode_kvwrite_fp8", "pkv_copy_to_device", "pkv_copy_to_host"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -410,3 +412,25 @@ class BlockManager:
         if st < 0:
             raise PagedKVError(st, "copy_on_write")
         return int(new.value), st == 1
+
+
+def copy_to_device(dst, src, stream=None) -> None:
+    """dst (CUDA tensor) <- src (CPU tensor, ideally pinned), same byte size, both
+    contiguous; asynchronous on the stream.  Pinned host memory is read by the SMs."""
+    if not (dst.is_cuda and not src.is_cuda and dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy_to_device needs a contiguous CUDA dst and a contiguous CPU src")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("size mismatch")
+    _check(lib().pkv_copy_to_device(_ptr(dst), _ptr(src), n, _stream_ptr(stream)), "copy_to_device")
+
+
+def copy_to_host(dst, src, stream=None) -> None:
+    """dst (CPU tensor, ideally pinned) <- src (CUDA tensor), same byte size, both
+    contiguous; asynchronous on the stream.  Pinned host memory is written by the SMs."""
+    if not (src.is_cuda and not dst.is_cuda and dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy_to_host needs a contiguous CPU dst and a contiguous CUDA src")
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("size mismatch")
+    _check(lib().pkv_copy_to_host(_ptr(dst), _ptr(src), n, _stream_ptr(stream)), "copy_to_host")

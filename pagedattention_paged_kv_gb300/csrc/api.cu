@@ -20,6 +20,7 @@ cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int64_t num_pairs,
                                int64_t num_blocks, int64_t block_bytes, int num_sms, int *err,
                                cudaStream_t stream);
+cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int num_sms, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_fp8(void *k_cache, void *v_cache, const void *k, const void *v,
                                          const int64_t *slot_mapping, int64_t num_tokens,
                                          int64_t num_slots, int row_elems, float k_scale,
@@ -338,6 +339,52 @@ extern "C" int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *bloc
     cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, num_blocks, block_bytes,
                                             d->sms, d->err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Host <-> device copies of a step's buffers, done by the SMs when the host side is
+// page-locked memory mapped into the device's address space (transfer.cu); other host
+// memory goes through cudaMemcpyAsync.  See pagedkv.h.
+static int step_copy(void *dst, const void *src, size_t bytes, void *stream, bool to_device) {
+    if (bytes == 0) return PKV_OK;
+    if (!dst || !src) return PKV_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    int st = device_info(&d);
+    if (st != PKV_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const void *host = to_device ? src : dst;
+    const void *devp = to_device ? dst : src;
+    cudaPointerAttributes da, ha;
+    if (cudaPointerGetAttributes(&da, devp) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    if (da.type != cudaMemoryTypeDevice || da.device != dev) return PKV_ERR_INVALID_ARG;
+    bool mapped = false;
+    if (cudaPointerGetAttributes(&ha, host) == cudaSuccess) {
+        mapped = ha.type == cudaMemoryTypeHost && ha.devicePointer != nullptr;
+    } else {
+        cudaGetLastError();
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!mapped) {
+        return cudaMemcpyAsync(dst, src, bytes, to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost, s) ==
+                       cudaSuccess
+                   ? PKV_OK
+                   : PKV_ERR_CUDA;
+    }
+    void *hdev = ha.devicePointer;  // the host buffer's address in the device's space
+    cudaError_t e = to_device ? pkv::launch_copy(dst, hdev, (int64_t)bytes, d->sms, s)
+                              : pkv::launch_copy(hdev, src, (int64_t)bytes, d->sms, s);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_to_device(void *dst, const void *src, size_t bytes, void *stream) {
+    return step_copy(dst, src, bytes, stream, true);
+}
+
+extern "C" int pkv_copy_to_host(void *dst, const void *src, size_t bytes, void *stream) {
+    return step_copy(dst, src, bytes, stream, false);
 }
 
 extern "C" size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,
