@@ -553,6 +553,17 @@ def pin_fp8_attention_equals_dequantised_bf16(orc):
     ref = orc.paged_attention(q, kb, vb, tables, cl, 0.25)
     assert np.all(np.isfinite(got))
     assert np.array_equal(got, ref), np.abs(got - ref).max()
+    # the same pools under varlen rows (prompt chunks at the end of each context, causal and
+    # not, single-token rows among them): still bit-identical to the dequantised bf16 oracle
+    q_lens = np.array([1, 5, 17, 1, 33], np.int64)
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    qv = normal_bf16(rng, (int(qsl[-1]), Hq, d))
+    for causal in (True, False):
+        got = orc.paged_attention_fp8(qv, kc, vc, k_scale, v_scale, tables, cl, 0.25, query_start_loc=qsl,
+                                      causal=causal)
+        ref = orc.paged_attention(qv, kb, vb, tables, cl, 0.25, query_start_loc=qsl, causal=causal)
+        assert np.all(np.isfinite(got))
+        assert np.array_equal(got, ref), np.abs(got - ref).max()
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
