@@ -110,8 +110,8 @@ int pkv_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const voi
  * pkv_workspace_size(PKV_OP_DECODE, ...) bytes, 256-byte aligned, contents
  * irrelevant on entry) holds the parts.  Calls that share a workspace must be
  * ordered on one stream.
- * Supported: dtype bf16, block_size 16, head_dim 64 or 128, num_heads a multiple
- * of num_kv_heads, group = num_heads / num_kv_heads <= 64, num_seqs <= 4096.
+ * Supported: dtype bf16, block_size 8, 16, 32 or 64, head_dim 64 or 128, num_heads a
+ * multiple of num_kv_heads, group = num_heads / num_kv_heads <= 64, num_seqs <= 4096.
  */
 int pkv_paged_attention_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *block_tables, const int32_t *context_lens,
@@ -209,7 +209,9 @@ int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *block_pairs, in
  * context_lens[s] keys.  q_len = 1 rows take the decode path; longer ones the
  * chunked-prefill path.  total_q_tokens = query_start_loc[num_seqs] and max_q_len
  * bounds every q_len (both as the caller knows them on the host).
- * Supported: as for decode, plus total_q_tokens <= 2^31 - 1.
+ * Supported: as for decode, plus total_q_tokens <= 2^31 - 1; rows with q_len >= 2
+ * need block_size 16 and group = num_heads / num_kv_heads <= 8 (PKV_ERR_UNSUPPORTED
+ * otherwise).
  */
 int pkv_paged_attention_varlen(void *out, const void *q, const int32_t *query_start_loc,
                                const void *k_cache, const void *v_cache,
