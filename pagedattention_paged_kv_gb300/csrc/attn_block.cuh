@@ -71,12 +71,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
-__device__ __forceinline__ float f16_lo(uint32_t v) {
-    return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
-}
-__device__ __forceinline__ float f16_hi(uint32_t v) {
-    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
-}
 
 template <int D>
 __device__ __forceinline__ void softmax_update(RowState<D> &st, float (&s)[2][4], uint32_t (&pa)[4]) {

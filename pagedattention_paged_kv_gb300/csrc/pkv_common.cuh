@@ -117,12 +117,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // ---- warp-level tensor-core fragments (mma.sync m16n8k16, bf16 -> fp32) ------
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                             uint32_t &r2, uint32_t &r3) {
@@ -172,7 +166,5 @@ __device__ __forceinline__ uint32_t swz128(int row, int col) {
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ uint32_t minu32(uint32_t a, uint32_t b) { return a < b ? a : b; }
-
-__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace pkv

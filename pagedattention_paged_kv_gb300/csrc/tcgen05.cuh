@@ -41,31 +41,11 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, in
            | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]; A is M rows on the TMEM lanes, two bf16 of a row per
-// 32-bit column (K = 16 takes 8 columns).  Issued by one thread.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-
-// Warp-wide forms: the whole (converged) warp executes the call with warp-uniform
-// operands and one lane, picked by elect.sync, issues.  Keeping the operands warp-uniform
+// D[tmem] (+)= A * B[smem], A from shared memory (umma_bf16_warp) or from TMEM
+// (umma_bf16_tmem_a_warp: M rows on the TMEM lanes, two 16-bit values of a row per 32-bit
+// column, K = 16 takes 8 columns); umma_commit_warp arrives once on `bar` when every
+// tcgen05 operation issued so far is done.  The whole (converged) warp executes the call
+// with warp-uniform operands and one lane, picked by elect.sync, issues.  Keeping the operands warp-uniform
 // lets them live in uniform registers; issuing from a single divergent thread instead
 // measured ~60-90 cycles per MMA on sm_103a (about the execution time of a
 // 128x128x16 MMA), against ~36 for this form.
@@ -96,13 +76,6 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t *bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
         ::"r"(smem_u32(bar))
         : "memory");
-}
-
-// Arrives once on `bar` when every tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
 }
 
 // Whole-warp TMEM allocation of `cols` columns; the base address lands in *slot.
