@@ -385,7 +385,7 @@ def run_trace(args, rank, world, local, dist):
     for r in W.request_stream(seed=seed, iterations=iters):
         by_iter.setdefault(r.arrival, []).append(r)
     stream = torch.cuda.current_stream()
-    times, kvb, flops, seq_steps, tokens = [], 0, 0, 0, 0
+    times, kvb, flops, seq_steps, tokens, launches = [], 0, 0, 0, 0, 0
     with ClockSampler(local) as clk:
         for it in range(iters):
             for r in by_iter.get(it, []):
@@ -407,6 +407,8 @@ def run_trace(args, rank, world, local, dist):
                 kvb += int(batch.context_lens[ql == 1].astype(np.int64).sum()) * Hkv * d * 4
                 flops += chunk_flops(batch.context_lens, ql, d, Hq)
                 seq_steps += int((ql == 1).sum())
+                # KV write, decode + merge, and prefill + merge when the batch has a chunk
+                launches += 3 + (2 if bool((ql >= 2).any()) else 0) + (1 if len(batch.copies) else 0)
                 tokens += batch.num_tokens
             eng.complete(batch)
     total_ms = max_over_ranks(sum(times), dist)
@@ -426,7 +428,7 @@ def run_trace(args, rank, world, local, dist):
         "decode_seq_steps_per_s": seq_steps / (total_ms * 1e-3), "tokens": tokens,
         "p50_us": float(np.percentile(times, 50)) * 1e3, "p99_us": float(np.percentile(times, 99)) * 1e3,
         "preemptions": eng.sched.total_preemptions, "finished": len(eng.sched.done),
-        "gpu_launches": 5 * len(times), "clocks": clk.summary(),
+        "gpu_launches": launches, "clocks": clk.summary(),
     }), flush=True)
 
 
