@@ -84,3 +84,56 @@ def test_block_manager_rejects_bad_free(lib):
     assert bm.num_free() == 2
     bm.free(ids)
     assert bm.num_free() == 4
+
+
+# ---- argument checks the C ABI makes on the host, before any device work ----------------
+
+def _c():
+    import ctypes
+    return ctypes
+
+
+def test_decode_rejects_bad_shapes_before_touching_the_device(lib):
+    c = _c()
+    vp = c.c_void_p
+    f = lib.pkv_paged_attention_decode
+    args = lambda Hq, Hkv, d, bs, dtype: [vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), 4, 2, Hq, Hkv, d, bs, 64,
+                                          c.c_float(0.1), dtype, vp(0), c.c_size_t(0), vp(0)]
+    assert f(*args(8, 3, 128, 16, 0)) == -1          # num_heads not a multiple of num_kv_heads
+    assert f(*args(8, 2, 96, 16, 0)) == -2           # head_dim 96
+    assert f(*args(8, 2, 128, 12, 0)) == -2          # block size 12
+    assert f(*args(8, 2, 128, 16, 7)) == -2          # dtype other than bf16
+    zero = [vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), 0, 2, 8, 2, 128, 16, 64, c.c_float(0.1), 0, vp(0),
+            c.c_size_t(0), vp(0)]
+    assert f(*zero) == 0                             # no sequences: nothing to do
+
+
+def test_fp8_calls_reject_bad_scales_and_head_dim_on_the_host(lib):
+    c = _c()
+    vp = c.c_void_p
+    def varlen_fp8(d, ks, vs):
+        return lib.pkv_paged_attention_varlen_fp8(vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), 2, 3, 2, 1, 8, 2,
+                                                  d, 16, 64, c.c_float(0.1), 1, c.c_float(ks), c.c_float(vs),
+                                                  vp(0), c.c_size_t(0), vp(0))
+    assert varlen_fp8(128, 0.0, 1.0) == -1
+    assert varlen_fp8(128, 1.0, float("nan")) == -1
+    assert varlen_fp8(128, float("inf"), 1.0) == -1
+    assert varlen_fp8(64, 1.0, 1.0) == -2
+    def decode_fp8(d, ks, vs):
+        return lib.pkv_paged_attention_decode_fp8(vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), 2, 1, 8, 2, d, 16, 64,
+                                                  c.c_float(0.1), c.c_float(ks), c.c_float(vs), vp(0),
+                                                  c.c_size_t(0), vp(0))
+    assert decode_fp8(128, -1.0, 1.0) == -1
+    assert decode_fp8(64, 1.0, 1.0) == -2
+    f = lib.pkv_reshape_and_cache_fp8
+    assert f(vp(0), vp(0), vp(0), vp(0), vp(0), 0, 4, 16, 2, 128, c.c_float(0.0), c.c_float(1.0), vp(0)) == -1
+    assert f(vp(0), vp(0), vp(0), vp(0), vp(0), 0, 4, 16, 2, 128, c.c_float(1.0), c.c_float(1.0), vp(0)) == 0
+    assert f(vp(0), vp(0), vp(0), vp(0), vp(0), 3, 4, 16, 2, 128, c.c_float(1.0), c.c_float(1.0), vp(0)) == -1
+
+
+def test_step_copies_check_arguments_on_the_host(lib):
+    c = _c()
+    vp = c.c_void_p
+    assert lib.pkv_copy_to_device(vp(0), vp(0), c.c_size_t(0), vp(0)) == 0     # nothing to copy
+    assert lib.pkv_copy_to_device(vp(0), vp(16), c.c_size_t(64), vp(0)) == -1  # no destination
+    assert lib.pkv_copy_to_host(vp(16), vp(0), c.c_size_t(64), vp(0)) == -1    # no source
