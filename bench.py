@@ -57,8 +57,10 @@ def parse():
                    help="tokens per pool block for the decode workloads (8, 16, 32, 64)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--graph-step", action="store_true",
-                   help="time the device step as a replayed CUDA graph of its launches")
+    p.add_argument("--eager-step", action="store_true",
+                   help="time the device step as eager library calls instead of replaying it from CUDA "
+                        "graphs (the default replays the captured launches, so no host work can fall "
+                        "between a step's events)")
     p.add_argument("--flush", choices=["read", "write", "none"], default="read",
                    help="between timed steps: read a 256 MB buffer (evicts the previous step's lines and "
                         "leaves L2 clean), write one (evicts them but leaves ~126 MB of dirty lines that "
@@ -224,6 +226,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def spread(ms):
+    """mean, p10, p50 and p90 of per-step times given in ms, in us."""
+    a = np.asarray(ms, dtype=np.float64) * 1e3
+    return {"mean": float(a.mean()), "p10": float(np.percentile(a, 10)), "p50": float(np.percentile(a, 50)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
 def kernel_source_sha(files):
     h = hashlib.sha256()
     for f in files:
@@ -277,11 +286,23 @@ def max_over_ranks(x, dist):
 # reference arm: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_step_time(b, seqs):
+def oracle_step_time(b, seqs, threads=None):
     """Times the oracle (as it stands) on the step restricted to `seqs` (all heads),
-    KV write of every new token included.  Returns (seconds, byte share of the sample)."""
+    KV write of every new token included, on `threads` host threads (all cores if None).
+    Returns (seconds, byte share of the sample, threads used)."""
     import oracle
     orc = oracle.load()
+    all_threads = orc.num_threads()
+    if threads is not None:
+        orc.set_num_threads(threads)
+    try:
+        return _oracle_step_time(orc, b, seqs)
+    finally:
+        if threads is not None:
+            orc.set_num_threads(all_threads)
+
+
+def _oracle_step_time(orc, b, seqs):
     mask = np.zeros(b.q.shape[0], np.uint8)
     qsl = b.query_start_loc if b.query_start_loc is not None else np.arange(b.num_seqs + 1)
     for s in seqs:
@@ -330,7 +351,11 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, **cfg, "seed": seed},
+        "config": {"workload": name, **cfg, "seed": seed,
+                   "reference_arm_bounds": {"steps_requested": args.steps, "steps_run": steps,
+                                            "steps_cap": 5, "warmup_requested": args.warmup,
+                                            "warmup_run": warmup, "warmup_cap": 1,
+                                            "sequences_per_step": len(seqs)}},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -370,9 +395,12 @@ class Packed:
 
 
 def run_trace(args, rank, world, local, dist):
-    """The continuous-batching trace: 300 scheduler iterations, each timed on the device
-    (KV write + one varlen attention call); reports per-iteration time and the
-    aggregate bytes/FLOPs of the whole trace."""
+    """The continuous-batching trace: 300 scheduler iterations.  Each iteration's host part
+    (scheduling, slot mapping, metadata and value copies to the device) runs first and is
+    timed on the host; then a 1 GB read evicts L2 and keeps the GPU busy while the host
+    enqueues the iteration's launches (block copies, KV write, one varlen attention call),
+    and CUDA events around those launches give the device time.  Reports the mean device
+    time per iteration (value) and, separately, the host time."""
     import torch
     from pagedattention_paged_kv_gb300 import workloads as W
     from pagedattention_paged_kv_gb300.engine import PagedKVEngine
@@ -385,21 +413,32 @@ def run_trace(args, rank, world, local, dist):
     for r in W.request_stream(seed=seed, iterations=iters):
         by_iter.setdefault(r.arrival, []).append(r)
     stream = torch.cuda.current_stream()
-    times, kvb, flops, seq_steps, tokens, launches = [], 0, 0, 0, 0, 0
+    flush_rd = torch.ones((1 << 30) // 8, dtype=torch.int64, device=f"cuda:{local}")
+    sink = torch.empty((), dtype=torch.int64, device=f"cuda:{local}")
+    times, host_prep, host_enq, kvb, flops, seq_steps, tokens, launches = [], [], [], 0, 0, 0, 0, 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for it in range(iters):
+            t0 = time.perf_counter()
             for r in by_iter.get(it, []):
                 eng.add(Sequence(r.req_id, r.prompt_len, r.output_len, r.arrival))
             batch = eng.schedule()
             if batch.num_seqs:
                 q, k, v = W.iteration_values(seed, it, batch.num_tokens, Hq, Hkv, d)
-                qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
-                kd = torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16)
-                vd = torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
+                prep = eng.prepare(batch, q, k, v)
                 torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t1 = time.perf_counter()
+                host_prep.append(t1 - t0)
+                torch.sum(flush_rd, dim=0, out=sink)
+                e0, e1 = evs[it]
                 e0.record(stream)
-                eng.run(batch, qd, kd, vd)
+                t2 = time.perf_counter()
+                eng.launch(prep)
+                host_enq.append(time.perf_counter() - t2)
                 e1.record(stream)
                 torch.cuda.synchronize()
                 times.append(e0.elapsed_time(e1))
@@ -407,13 +446,13 @@ def run_trace(args, rank, world, local, dist):
                 kvb += int(batch.context_lens[ql == 1].astype(np.int64).sum()) * Hkv * d * 4
                 flops += chunk_flops(batch.context_lens, ql, d, Hq)
                 seq_steps += int((ql == 1).sum())
-                # KV write, decode + merge, and prefill + merge when the batch has a chunk
-                launches += 3 + (2 if bool((ql >= 2).any()) else 0) + (1 if len(batch.copies) else 0)
+                launches += eng.launches(batch)
                 tokens += batch.num_tokens
             eng.complete(batch)
     total_ms = max_over_ranks(sum(times), dist)
     if rank != 0:
         return
+    frag = eng.sched.fragmentation_report()
     print(json.dumps({
         "metric": "continuous-batching trace: device time per iteration", "value": total_ms / len(times) * 1e3,
         "unit": "us/iteration", "higher_is_better": False, "n_gpus": world, "steps": len(times), "warmup": 0,
@@ -422,12 +461,18 @@ def run_trace(args, rank, world, local, dist):
         "config": {"workload": "cb_trace_300_iterations", "arrivals": "Poisson(4) per iteration",
                    "prompt": "log-normal mean 1500 std 600, cap 8192", "output": "uniform[16,512]",
                    "max_running": 128, "chunk": 512, "num_blocks": NB, "num_heads": Hq, "num_kv_heads": Hkv,
-                   "head_dim": d, "seed": seed},
+                   "head_dim": d, "seed": seed,
+                   "l2": "a 1 GB read before each iteration's launches (evicts L2; the host enqueues meanwhile)"},
+        "device_time": "CUDA events around the iteration's library launches only (block copies, KV write, "
+                       "attention); scheduling, slot mapping and the metadata copies run before, on the host",
+        "iteration_us": spread(times), "host_prepare_us": spread(host_prep),
+        "host_enqueue_us": spread(host_enq),
         "total_ms": total_ms, "decode_kv_gbs": kvb / (total_ms * 1e-3) / 1e9,
         "chunk_tflops_over_total_time": flops / (total_ms * 1e-3) / 1e12,
         "decode_seq_steps_per_s": seq_steps / (total_ms * 1e-3), "tokens": tokens,
         "p50_us": float(np.percentile(times, 50)) * 1e3, "p99_us": float(np.percentile(times, 99)) * 1e3,
         "preemptions": eng.sched.total_preemptions, "finished": len(eng.sched.done),
+        "fragmentation": frag,
         "gpu_launches": launches, "clocks": clk.summary(),
     }), flush=True)
 
@@ -525,30 +570,46 @@ def main():
         if ev is not None:
             ev[2].record(stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    # Timed steps run on one stream: flush, event, KV write, event, attention, event.  By
+    # default the KV write and the attention call are each replayed from a CUDA graph
+    # captured once (the same launches as the eager calls), and every event object is
+    # created before the loop, so no host work (argument marshalling, descriptor
+    # encoding, lazy event creation) can sit between a step's events while the GPU idles.
+    ts = torch.cuda.Stream()
+    ts.wait_stream(stream)
+    with torch.cuda.stream(ts):
+        for _ in range(max(3, args.warmup)):
+            step()
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
+    kv_graph = attn_graph = None
+    if not args.eager_step:
+        from pagedattention_paged_kv_gb300.graph import CapturedStep
+        kv_graph = None if fused else CapturedStep(kv_write, stream=ts)
+        attn_graph = CapturedStep(attention, stream=ts)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e3 in events:       # create the CUDA events now, outside the timed region
+        for e in e3:
+            e.record(ts)
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    cap_step = None
-    if args.graph_step:
-        from pagedattention_paged_kv_gb300.graph import CapturedStep
-        cap_step = CapturedStep(step)
     with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            l2_flush(i)
-            if cap_step is None:
-                step(events[i])
-            else:
-                cap_step.stream.wait_stream(stream)
-                events[i][0].record(cap_step.stream)
-                events[i][1].record(cap_step.stream)
-                cap_step.replay()
-                events[i][2].record(cap_step.stream)
-                stream.wait_stream(cap_step.stream)
+        with torch.cuda.stream(ts):
+            for i in range(args.steps):
+                l2_flush(i)
+                events[i][0].record(ts)
+                if kv_graph is not None:
+                    kv_graph.replay()
+                elif args.eager_step:
+                    kv_write()
+                events[i][1].record(ts)
+                if attn_graph is not None:
+                    attn_graph.replay()
+                else:
+                    attention()
+                events[i][2].record(ts)
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -664,6 +725,10 @@ def main():
         "kv_write_us": 1e3 * sum(kv_ms) / len(kv_ms),
         "kv_write": "fused into the decode launch" if fused else "separate launch",
         "attention_us": 1e3 * t_attn,
+        "timing": {"method": ("eager library calls" if args.eager_step else
+                              "each timed step replays the captured KV-write and attention graphs") +
+                             " on one stream between CUDA events created before the loop",
+                   "step_us": spread(step_ms), "attention_us": spread(attn_ms)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -686,6 +751,12 @@ def main():
             "value": total_bytes * share / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {min(32, b.num_seqs)} of {b.num_seqs} sequences (all heads, KV write of "
                       f"every new token), one step, bytes scaled by their share of the total context"}
+        if args.config in ("tiny_decode", "gqa_decode"):
+            n1 = min(8, b.num_seqs)
+            dt1, share1, c1 = oracle_step_time(b, sample_seqs(b, n1), threads=1)
+            line["cpu_baseline"]["single_thread"] = {
+                "value": total_bytes * share1 / dt1 / 1e9, "unit": "GB/s", "cores": c1,
+                "sample": f"first {n1} of {b.num_seqs} sequences, one step, one host thread"}
     print(json.dumps(line), flush=True)
 
 

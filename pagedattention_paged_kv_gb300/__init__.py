@@ -333,6 +333,13 @@ def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
                                  bs, Hkv, d, dt, _stream_ptr(stream)), "copy_blocks")
 
 
+def attention_launches(max_q_len: int) -> int:
+    """Kernels one paged_attention_varlen call launches for a batch whose longest q_len is
+    max_q_len: the decode kernel and its merge, plus the chunked-prefill kernel and its
+    merge when some sequence has q_len >= 2."""
+    return 2 if max_q_len < 2 else 4
+
+
 def get_device_error(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the device error flags."""
     r = lib().pkv_get_device_error(_stream_ptr(stream))

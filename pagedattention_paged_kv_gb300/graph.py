@@ -11,10 +11,11 @@ from __future__ import annotations
 
 
 class CapturedStep:
-    def __init__(self, fn, warmup: int = 2):
+    def __init__(self, fn, warmup: int = 2, stream=None):
+        """`stream`: the (non-default) stream to capture and replay on; a new one if None."""
         import torch
         self.torch = torch
-        self.stream = torch.cuda.Stream()
+        self.stream = stream if stream is not None else torch.cuda.Stream()
         self.stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(self.stream):
             for _ in range(warmup):  # first calls set up per-device state outside capture

@@ -21,6 +21,22 @@ when it has produced output_len tokens, one per decode step; the last prefill ch
 produces no token; a preempted sequence recomputes its prompt and the tokens it had
 already produced as one longer prefill; the waiting queue is FIFO; running sequences
 keep their admission order in the batch.
+
+Token budget (the lesson's "Exercises": add --max-num-batched-tokens to the toy
+scheduler).  When max_num_batched_tokens is set, an iteration schedules at most that
+many new tokens: every running decode first (one token each, so a long prompt's chunk
+never delays the decodes -- the inter-token latency that chunked prefill is there to
+protect), then the prefilling sequences in admission order, each taking
+min(chunk, tokens it still needs, budget left).  The budget must be at least
+max_num_seqs, so the decodes always fit and, whenever a sequence is prefilling, at
+least one token is left for it: every sequence keeps making progress.
+
+Fragmentation report (the lesson's fragmentation exercise, measured instead of
+computed): after every forward pass the scheduler records the slots its running
+sequences hold in their blocks, the tokens whose K/V those slots store, and the slots
+reserved for prompt tokens not yet computed; the rest is internal fragmentation, at
+most block_size - 1 slots per sequence.  When a sequence finishes, the slots it held
+and the tokens it stored are added to run-wide totals.
 """
 from __future__ import annotations
 
@@ -162,10 +178,27 @@ class PrefixCache:
         return freed
 
 
+@dataclass
+class FragmentationSample:
+    """KV slot accounting of the running sequences after one forward pass."""
+    iteration: int
+    slots_held: int       # slots in the blocks the running sequences hold
+    tokens_stored: int    # tokens whose K/V are in those slots
+    tokens_reserved: int  # slots kept for prompt tokens not computed yet (chunked prefill)
+    max_seq_wasted: int   # the largest number of wasted slots of one sequence
+
+    @property
+    def wasted(self) -> int:
+        return self.slots_held - self.tokens_stored - self.tokens_reserved
+
+
 class Scheduler:
     def __init__(self, block_manager: BlockManager, max_num_seqs: int = 128, chunk_size: int = 512,
                  block_size: int = BLOCK_SIZE, max_num_batched_tokens: int | None = None,
                  prefix_cache: bool = False):
+        if max_num_batched_tokens is not None and max_num_batched_tokens < max_num_seqs:
+            raise ValueError("max_num_batched_tokens must be >= max_num_seqs (every running decode "
+                             "gets its token before any prefill chunk)")
         self.bm = block_manager
         self.cache = PrefixCache(block_manager, block_size) if prefix_cache else None
         self._copies: list = []
@@ -178,6 +211,9 @@ class Scheduler:
         self.done: list[Sequence] = []
         self.iteration = 0
         self.total_preemptions = 0
+        self.fragmentation: list[FragmentationSample] = []
+        self.released_slots = 0    # slots held by finished sequences when they were released
+        self.released_tokens = 0   # tokens those sequences had stored
 
     # -- queue -------------------------------------------------------------------
     def add(self, seq: Sequence) -> None:
@@ -239,6 +275,8 @@ class Scheduler:
         keep = []
         for s in self.running:
             if s.finished:
+                self.released_slots += len(s.block_table) * self.block_size
+                self.released_tokens += s.computed
                 self.bm.free(s.block_table)
                 s.block_table = []
                 self.done.append(s)
@@ -286,23 +324,27 @@ class Scheduler:
             self.waiting.pop(0)
             self.running.append(s)
             admitted += 1
-        # (4) one chunk or one decode token per running sequence
-        items = []
+        # (4) one chunk or one decode token per running sequence; under a token budget the
+        # decodes are served first, then the chunks in admission order
         budget = self.max_num_batched_tokens
+        take = {}
+        if budget is not None:
+            for s in self.running:
+                if not s.in_prefill:
+                    take[id(s)] = 1
+                    budget -= 1
+            assert budget >= 0  # running <= max_num_seqs <= max_num_batched_tokens
         for s in self.running:
             if s.in_prefill:
                 n = min(self.chunk_size, s.prefill_target - s.computed)
                 if budget is not None:
                     n = min(n, budget)
-                    if n <= 0:
-                        continue
-            else:
-                n = 1
-                if budget is not None and budget < 1:
-                    continue
-            items.append(ScheduledItem(s, s.computed, n))
-            if budget is not None:
-                budget -= n
+                    budget -= n
+                if n > 0:
+                    take[id(s)] = n
+            elif budget is None:
+                take[id(s)] = 1
+        items = [ScheduledItem(s, s.computed, take[id(s)]) for s in self.running if id(s) in take]
         self.iteration += 1
         batch = self._pack(items, admitted, finished, preempted)
         if self._copies:
@@ -321,6 +363,15 @@ class Scheduler:
                 s.decoded += 1
             if self.cache is not None and s.prompt_tokens is not None and not was_decode:
                 self.cache.insert(s.prompt_tokens, s.block_table, min(s.computed, s.prompt_len) // self.block_size)
+        held = stored = reserved = worst = 0
+        for s in self.running:
+            h = len(s.block_table) * self.block_size
+            r = max(0, s.prefill_target - s.computed)
+            held += h
+            stored += s.computed
+            reserved += r
+            worst = max(worst, h - s.computed - r)
+        self.fragmentation.append(FragmentationSample(self.iteration, held, stored, reserved, worst))
 
     def _pack(self, items, admitted, finished, preempted) -> IterationBatch:
         S = len(items)
@@ -341,6 +392,22 @@ class Scheduler:
     # -- accounting ----------------------------------------------------------------
     def blocks_in_use(self) -> int:
         return sum(len(s.block_table) for s in self.running)
+
+    def fragmentation_report(self) -> dict:
+        """Internal fragmentation measured over the run: per iteration (mean and worst share
+        of held slots that store nothing and are reserved for nothing) and at release
+        (slots the finished sequences held minus the tokens they stored)."""
+        per_iter = [f.wasted / f.slots_held for f in self.fragmentation if f.slots_held]
+        return {
+            "iterations": len(self.fragmentation),
+            "mean_wasted_share": float(np.mean(per_iter)) if per_iter else 0.0,
+            "max_wasted_share": float(np.max(per_iter)) if per_iter else 0.0,
+            "max_wasted_slots_per_seq": max((f.max_seq_wasted for f in self.fragmentation), default=0),
+            "released_slots": self.released_slots,
+            "released_tokens": self.released_tokens,
+            "released_wasted_share": (1.0 - self.released_tokens / self.released_slots)
+            if self.released_slots else 0.0,
+        }
 
     def slot_waste(self) -> list:
         """Per running sequence: slots its blocks hold beyond the tokens they are held

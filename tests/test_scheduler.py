@@ -135,3 +135,120 @@ def test_fragmentation_exercise():
     assert lo <= contiguous <= 0.85          # ~0.82 for these lengths (the lesson quotes 60-80%)
     assert paged < g["paged_waste_below"]    # well under 4%: ~bs/2 slots per request
     assert np.all(np.ceil(lengths / bs) * bs - lengths <= bs - 1)
+
+
+def test_token_budget_decodes_first_and_drains():
+    """--max-num-batched-tokens (the lesson's "Exercises"): no iteration schedules more
+    tokens than the budget, every running decode gets its token in every iteration (a
+    prefill chunk never delays a decode), prefill chunks take what is left in admission
+    order, and the whole stream still finishes."""
+    budget = 640
+    seen_prefill_progress = []
+
+    def check(sch, bm, batch, phase):
+        if phase != "scheduled":
+            return
+        assert batch.num_tokens <= budget
+        scheduled = {id(it.seq): it for it in batch.items}
+        for s in sch.running:
+            if not s.in_prefill:
+                assert id(s) in scheduled and scheduled[id(s)].q_len == 1, "a decode was skipped"
+        prefills = [s for s in sch.running if s.in_prefill]
+        if prefills:
+            # the first prefilling sequence in admission order always gets tokens
+            assert id(prefills[0]) in scheduled
+            seen_prefill_progress.append(scheduled[id(prefills[0])].q_len)
+            # chunks are granted in admission order: a later chunk only when earlier ones got
+            # all they asked for
+            short = False
+            for s in prefills:
+                want = min(512, s.prefill_target - s.computed)
+                got = scheduled[id(s)].q_len if id(s) in scheduled else 0
+                assert not (short and got > 0), "a later chunk was served before an earlier one"
+                short = short or got < want
+
+    reqs = W.request_stream(seed=5002, iterations=120)
+    bm = pkv.BlockManager(65536)
+    sch = Scheduler(bm, max_num_seqs=128, chunk_size=512, max_num_batched_tokens=budget)
+    by_iter = {}
+    for r in reqs:
+        by_iter.setdefault(r.arrival, []).append(r)
+    it = 0
+    while it < 120 or sch.running or sch.waiting:
+        for r in by_iter.get(it, []):
+            sch.add(Sequence(r.req_id, r.prompt_len, r.output_len, r.arrival))
+        batch = sch.schedule()
+        check(sch, bm, batch, "scheduled")
+        sch.complete(batch)
+        it += 1
+        assert it < 20000, "trace does not drain under the budget"
+    assert len(sch.done) == len(reqs) and bm.num_free() == 65536
+    for s in sch.done:
+        assert s.decoded == s.output_len
+    assert min(seen_prefill_progress) >= 1
+    assert any(n < 512 for n in seen_prefill_progress), "the budget never cut a chunk"
+
+
+def test_token_budget_tight_budget_still_progresses():
+    # budget == max_num_seqs: when every slot decodes nothing is left for prefill, yet any
+    # prefilling sequence gets at least one token (running <= max_num_seqs - 1 decodes)
+    bm = pkv.BlockManager(4096)
+    sch = Scheduler(bm, max_num_seqs=4, chunk_size=512, max_num_batched_tokens=4)
+    for i in range(6):
+        sch.add(Sequence(i, 40 + 7 * i, 3))
+    for _ in range(2000):
+        b = sch.schedule()
+        assert b.num_tokens <= 4
+        sch.complete(b)
+        if not sch.running and not sch.waiting:
+            break
+    assert len(sch.done) == 6 and bm.num_free() == 4096
+
+
+def test_token_budget_below_max_num_seqs_is_refused():
+    with pytest.raises(ValueError):
+        Scheduler(pkv.BlockManager(16), max_num_seqs=8, max_num_batched_tokens=7)
+
+
+def test_fragmentation_report_measured_by_the_scheduler():
+    """The lesson's fragmentation exercise (1000 requests, lengths with mean 1500 and std
+    600), measured by the scheduler from the blocks it actually held: request i holds
+    L_i tokens when it finishes (prompt L_i - 1, one output token), so the slots held at
+    release minus the tokens stored must equal the closed form sum(ceil(L/16)*16 - L), and
+    no sequence ever wastes more than block_size - 1 slots."""
+    g = GOLDEN["fragmentation_exercise"]
+    lengths = np.minimum(W.length_sample(5001, g["requests"], g["mean_tokens"], g["std_tokens"]), g["cap_tokens"])
+    lengths = lengths[lengths >= 2]  # a request needs a prompt token and an output token
+    bs = g["block_size"]
+    bm = pkv.BlockManager(200000)
+    sch = Scheduler(bm, max_num_seqs=256, chunk_size=512)
+    for i, L in enumerate(lengths):
+        sch.add(Sequence(i, int(L) - 1, 1))
+    n = 0
+    while sch.running or sch.waiting:
+        b = sch.schedule()
+        sch.complete(b)
+        n += 1
+        assert n < 10000
+    rep = sch.fragmentation_report()
+    slots = int((np.ceil(lengths / bs) * bs).sum())
+    assert rep["released_tokens"] == int(lengths.sum())
+    assert rep["released_slots"] == slots
+    closed = 1.0 - lengths.sum() / slots
+    assert rep["released_wasted_share"] == pytest.approx(closed, rel=0, abs=1e-15)
+    assert rep["released_wasted_share"] < g["paged_waste_below"]
+    assert 0 <= rep["max_wasted_slots_per_seq"] <= bs - 1
+    assert rep["iterations"] == n
+    for f in sch.fragmentation:
+        assert f.wasted >= 0 and f.tokens_stored + f.tokens_reserved <= f.slots_held
+
+
+def test_fragmentation_report_on_the_trace():
+    # per-iteration accounting over the 300-iteration trace stays within a block per sequence
+    sch, bm, reqs = run_trace(65536)
+    rep = sch.fragmentation_report()
+    assert 0 < rep["mean_wasted_share"] < 0.04
+    assert rep["max_wasted_slots_per_seq"] <= 15
+    lens = np.array([s.prompt_len + s.output_len for s in sch.done])
+    assert rep["released_tokens"] == int(lens.sum())
+    assert rep["released_slots"] == int((np.ceil(lens / 16) * 16).sum())
