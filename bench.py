@@ -578,7 +578,7 @@ def main():
     ts = torch.cuda.Stream()
     ts.wait_stream(stream)
     with torch.cuda.stream(ts):
-        for _ in range(max(3, args.warmup)):
+        for _ in range(2):  # set-up calls (per-device state, a check of the device flags)
             step()
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
@@ -595,20 +595,33 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    def run_step():
+        if kv_graph is not None:
+            kv_graph.replay()
+        elif args.eager_step:
+            kv_write()
+
+    def run_attention():
+        if attn_graph is not None:
+            attn_graph.replay()
+        else:
+            attention()
+
+    warmup = max(3, args.warmup)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(ts):
+            # the warm-up steps run right before the timed ones (after the clock sampler has
+            # started), so the GPU does not sit idle between them
+            for i in range(warmup):
+                l2_flush(i)
+                run_step()
+                run_attention()
             for i in range(args.steps):
                 l2_flush(i)
                 events[i][0].record(ts)
-                if kv_graph is not None:
-                    kv_graph.replay()
-                elif args.eager_step:
-                    kv_write()
+                run_step()
                 events[i][1].record(ts)
-                if attn_graph is not None:
-                    attn_graph.replay()
-                else:
-                    attention()
+                run_attention()
                 events[i][2].record(ts)
         torch.cuda.synchronize()
     if dist is not None:
@@ -702,10 +715,10 @@ def main():
 
     if rank != 0:
         return
-    launches_per_step = (0 if fused else 1) + (2 if not varlen else (4 if max_q_len >= 2 else 2))
+    launches_per_step = (0 if fused else 1) + (2 if not varlen else pkv.attention_launches(max_q_len))
     line = {
         "metric": METRIC if args.config == "gqa_decode" else f"{name}: HBM GB/s of the step",
-        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
         "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 kv / f16 mma / f32 acc" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, random block permutation" +
@@ -745,6 +758,7 @@ def main():
             "algorithmic_bytes": attn_bytes}
     else:
         line.update(parts)
+        overlap_figures(line)
     if not args.no_cpu_baseline:
         dt, share, cores = oracle_step_time(b, sample_seqs(b, 32))
         line["cpu_baseline"] = {
@@ -801,7 +815,9 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, config
             res["chunk_us"] = t * 1e3
             res["chunk_tflops"] = tf
             traffic = recorded_traffic("prefill_fp8" if fp8 else "prefill", PREFILL_SOURCES, config)
-            res["roofline"] = {"bound": "tensor", "kernel": "paged_prefill_kernel (+ merge, timed together)",
+            res["roofline"] = {"bound": "tensor",
+                               "kernel": "paged_varlen_kernel on a chunk-only batch (its prefill CTAs; "
+                                         "+ merges, timed together)",
                                "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
                                "peak_source": "measured bf16_tflops (burst cuBLAS)" + (
                                    " x 1: the fp16 MMAs of the FP8 cache run at the bf16 dense rate"
@@ -813,6 +829,15 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, config
             res["decodes_us"] = t * 1e3
             res["decodes_gbs"] = byts / (t * 1e-3) / 1e9
     return res
+
+
+def overlap_figures(line):
+    """How the mixed step compares with its parts run alone: the step's attention call
+    over the longer part (1.0 = the shorter part fully hidden) and over their sum."""
+    if "chunk_us" in line and "decodes_us" in line:
+        a = line["attention_us"]
+        line["attention_over_max_of_parts"] = a / max(line["chunk_us"], line["decodes_us"])
+        line["attention_over_sum_of_parts"] = a / (line["chunk_us"] + line["decodes_us"])
 
 
 if __name__ == "__main__":

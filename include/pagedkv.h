@@ -45,6 +45,13 @@
  *     than context_len) cannot be seen by the host: the kernels skip the bad
  *     item, never read or write outside the caller's buffers, and record a flag
  *     in a device error word that pkv_get_device_error returns.
+ *   - Per-device state: on its first call on a device (with that device current) the
+ *     library looks up facts it then keeps for the life of the process -- the SM count,
+ *     the shared-memory limit, and the device addresses of its own device variables
+ *     (the error word, the static scratch array).  These lookups assume the device's
+ *     primary context is never reset or destroyed while the library is loaded
+ *     (cudaDeviceReset, or a context torn down and created again, would leave the kept
+ *     addresses stale).  Make the first call on a device before any stream capture.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -290,6 +297,18 @@ int pkv_paged_attention_decode_static(void *out, const void *q, const void *k_ca
  */
 int pkv_copy_to_device(void *dst, const void *src, size_t bytes, void *stream);
 int pkv_copy_to_host(void *dst, const void *src, size_t bytes, void *stream);
+
+/*
+ * Limit, in nanoseconds, of every pipeline wait inside the attention kernels launched
+ * from now on (a consumer warp waiting for its K/V stage, a producer for a free stage).
+ * A wait that runs out sets PKV_DEVERR_TIMEOUT, stops its CTA's pipeline, lets the
+ * copies and tensor-core operations the CTA already issued complete, and the kernel
+ * returns: the GPU context stays usable and pkv_get_device_error reports the flag.
+ * Default 2 s (also restored by limit_ns = 0); a wait that ends normally takes
+ * microseconds.  A short limit makes healthy launches give up too -- it exists so tests
+ * can exercise the failure path.  Not from the pages.
+ */
+void pkv_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Workspace bytes the op needs on the current device for these sizes (0 if the
  * sizes are unsupported).  Does not allocate. */

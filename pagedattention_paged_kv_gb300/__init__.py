@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_block_manager_copy_on_write.argtypes = [vp, ctypes.c_int32, vp]
         L.pkv_copy_to_device.argtypes = [vp, vp, sz, vp]
         L.pkv_copy_to_host.argtypes = [vp, vp, sz, vp]
+        L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.pkv_set_wait_limit_ns.restype = None
         L.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.pkv_workspace_size.restype = sz
         L.pkv_status_string.argtypes = [i32]
@@ -335,9 +337,16 @@ def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
 
 def attention_launches(max_q_len: int) -> int:
     """Kernels one paged_attention_varlen call launches for a batch whose longest q_len is
-    max_q_len: the decode kernel and its merge, plus the chunked-prefill kernel and its
-    merge when some sequence has q_len >= 2."""
-    return 2 if max_q_len < 2 else 4
+    max_q_len: the decode kernel and its merge; or, when some sequence has q_len >= 2, the
+    one varlen kernel (decode and prefill CTAs) and the two merges."""
+    return 2 if max_q_len < 2 else 3
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of the kernels' pipeline waits for launches from now on (0: the default,
+    2 s).  A wait that runs out flags DEVERR_TIMEOUT and the kernel returns; short limits
+    exist to test that failure path."""
+    lib().pkv_set_wait_limit_ns(int(limit_ns))
 
 
 def get_device_error(stream=None) -> int:

@@ -8,9 +8,12 @@
 #include <cstring>
 #include <mutex>
 
+#include <atomic>
+
 #include "../../include/pagedkv.h"
 #include "paged_decode.cuh"
 #include "paged_prefill.cuh"
+#include "paged_varlen.cuh"
 
 namespace pkv {
 cudaError_t launch_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
@@ -45,6 +48,20 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
+
+// Limit of a kernel's pipeline waits (pkv_set_wait_limit_ns); read at each launch.
+std::atomic<uint64_t> g_wait_ns{pkv::kWaitTimeoutNs};
+
+// Measured GB300 rates behind the varlen grid split (paged_varlen.cu).  A decode CTA that
+// shares the GPU with prefill CTAs streams ~70 GB/s of bf16 K/V (~42 GB/s of FP8 codes);
+// alone, a few decode CTAs reach ~90 (~48) GB/s each.  The whole decode saturates near
+// 5.9 TB/s; a prefill CTA sustains ~7.8 TFLOP/s of causal attention.  On the 512-token
+// chunk + 127 decodes step these rates put the split at the measured optimum (36 of 152
+// CTAs decode with a bf16 cache, 32 with an FP8 one).
+constexpr float kDecodeBytesPerUsSm = 70e3f;
+constexpr float kDecodeBytesPerUsSmFp8 = 42e3f;
+constexpr float kDecodeBytesPerUsGpu = 5.9e6f;
+constexpr float kPrefillFlopPerUsSm = 7.8e6f;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -188,18 +205,17 @@ int check_common(int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv
     return PKV_OK;
 }
 
-// Runs the decode kernel on the sequences selected by `query_start_loc` (all if null).
-int run_decode(void *out, const void *q, const int32_t *query_start_loc, int total_q,
-               const void *k_cache,
-               const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
-               int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
-               int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
-               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, int block_size,
-               bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f, const void *k_new = nullptr,
-               const void *v_new = nullptr) {
+// The decode kernel's tensor maps and arguments for the sequences selected by
+// `query_start_loc` (all if null).
+int prepare_decode(pkv::DecodeArgs &a, CUtensorMap &kmap, CUtensorMap &vmap, void *out, const void *q,
+                   const int32_t *query_start_loc, int total_q, const void *k_cache,
+                   const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                   int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+                   int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
+                   const DeviceInfo &d, const DecodePlan &p, int block_size, bool fp8, float k_scale,
+                   float v_scale, const void *k_new, const void *v_new) {
     if (ws_bytes < p.bytes || !ws) return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(ws, 256)) return PKV_ERR_INVALID_ARG;
-    CUtensorMap kmap, vmap;
     const int box_heads = block_size < kBlockSize ? 1 : p.heads_per_cta;
     int st = encode_cache_map(&kmap, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box_heads,
                               fp8);
@@ -207,7 +223,6 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
         st = encode_cache_map(&vmap, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box_heads,
                               fp8);
     if (st != PKV_OK) return st;
-    pkv::DecodeArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_tables = block_tables;
@@ -238,6 +253,27 @@ int run_decode(void *out, const void *q, const int32_t *query_start_loc, int tot
     a.ws_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
     a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
     a.err = d.err;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+// Runs the decode kernel (and its merge) on the sequences selected by `query_start_loc`
+// (all if null).
+int run_decode(void *out, const void *q, const int32_t *query_start_loc, int total_q,
+               const void *k_cache,
+               const void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+               int num_seqs, int max_blocks_per_seq, int num_heads, int num_kv_heads,
+               int head_dim, int64_t num_blocks, float scale, uint8_t *ws, size_t ws_bytes,
+               const DeviceInfo &d, const DecodePlan &p, cudaStream_t stream, int block_size,
+               bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f, const void *k_new = nullptr,
+               const void *v_new = nullptr) {
+    pkv::DecodeArgs a;
+    CUtensorMap kmap, vmap;
+    const int st = prepare_decode(a, kmap, vmap, out, q, query_start_loc, total_q, k_cache, v_cache,
+                                  block_tables, context_lens, num_seqs, max_blocks_per_seq, num_heads,
+                                  num_kv_heads, head_dim, num_blocks, scale, ws, ws_bytes, d, p, block_size,
+                                  fp8, k_scale, v_scale, k_new, v_new);
+    if (st != PKV_OK) return st;
     return pkv::launch_paged_decode(head_dim, fp8, kmap, vmap, a, p.smem, stream) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
@@ -270,6 +306,10 @@ extern "C" int pkv_get_device_error(void *stream) {
     if (cudaMemsetAsync(d->err, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
     return h;
+}
+
+extern "C" void pkv_set_wait_limit_ns(uint64_t limit_ns) {
+    g_wait_ns.store(limit_ns == 0 ? pkv::kWaitTimeoutNs : limit_ns, std::memory_order_relaxed);
 }
 
 extern "C" int pkv_reshape_and_cache(void *k_cache, void *v_cache, const void *k, const void *v,
@@ -567,12 +607,20 @@ static int varlen(void *out, const void *q, const int32_t *query_start_loc, cons
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE_TOO_SMALL;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Single-token rows: the decode kernel (it skips every other sequence).
-    st = run_decode(out, q, query_start_loc, total_q_tokens, k_cache, v_cache, block_tables, context_lens,
-                    num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim, num_blocks,
-                    scale, ws, p.bytes, *d, p, s, block_size, fp8, k_scale, v_scale);
-    if (st != PKV_OK || !prefill_rows) return st;
-    // Multi-token rows (prefill chunks): the chunked-prefill kernel.
+    if (!prefill_rows)  // single-token rows only: the decode kernel
+        return run_decode(out, q, query_start_loc, total_q_tokens, k_cache, v_cache, block_tables,
+                          context_lens, num_seqs, max_blocks_per_seq, num_heads, num_kv_heads, head_dim,
+                          num_blocks, scale, ws, p.bytes, *d, p, s, block_size, fp8, k_scale, v_scale);
+    // Decode rows and prefill chunks: one launch whose CTAs split between the two
+    // (paged_varlen.cu); the decode side skips sequences with q_len != 1, the prefill
+    // side those with q_len < 2.
+    pkv::DecodeArgs ad;
+    CUtensorMap dkmap, dvmap;
+    st = prepare_decode(ad, dkmap, dvmap, out, q, query_start_loc, total_q_tokens, k_cache, v_cache,
+                        block_tables, context_lens, num_seqs, max_blocks_per_seq, num_heads, num_kv_heads,
+                        head_dim, num_blocks, scale, ws, p.bytes, *d, p, block_size, fp8, k_scale, v_scale,
+                        nullptr, nullptr);
+    if (st != PKV_OK) return st;
     CUtensorMap qmap, kmap, vmap;
     // one box per tile half
     st = encode_q_map(&qmap, q, total_q_tokens, num_heads, head_dim, pp.group, pp.tokens_per_tile / 2);
@@ -607,7 +655,18 @@ static int varlen(void *out, const void *q, const int32_t *query_start_loc, cons
     a.ws_o = reinterpret_cast<float *>(pws + pp.off_o);
     a.max_seqs = num_seqs;
     a.err = d->err;
-    return pkv::launch_paged_prefill(head_dim, fp8, qmap, kmap, vmap, a, pp, s) == cudaSuccess
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    // unit costs for the grid split
+    const float dec_unit_bytes = (float)kBlockSize * p.heads_per_cta * head_dim * (fp8 ? 1 : 2) * 2;
+    const float pre_unit_flops = 4.f * head_dim * kBlockSize * pp.rows;
+    pkv::VarlenSplit sp;
+    sp.dec_sm_us = dec_unit_bytes / (fp8 ? kDecodeBytesPerUsSmFp8 : kDecodeBytesPerUsSm);
+    sp.dec_gpu_us = dec_unit_bytes / kDecodeBytesPerUsGpu;
+    sp.pre_sm_us = pre_unit_flops / kPrefillFlopPerUsSm;
+    const size_t smem = p.smem > pp.smem ? p.smem : pp.smem;
+    if (smem > (size_t)d->smem_optin || p.grid != pp.grid) return PKV_ERR_UNSUPPORTED;
+    return pkv::launch_paged_varlen(head_dim, fp8, dkmap, dvmap, ad, qmap, kmap, vmap, a, pp, sp, smem, s) ==
+                   cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
 }

@@ -7,6 +7,8 @@
 // `chunk_stride` the distance between sub-tiles.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "pkv_common.cuh"
@@ -163,6 +165,30 @@ __device__ __forceinline__ void finish_sums(RowState<D> &st) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The dynamic shared memory a kernel has been allowed on each device (one record per
+// kernel, kept by its launcher).
+struct SmemAllowance {
+    std::atomic<int> bytes[64];
+};
+
+// Raises `kernel`'s dynamic shared-memory limit to `smem` on the current device unless an
+// earlier call already allowed at least that much, so the attribute call leaves the
+// per-launch path after a kernel's first launch on a device.
+template <typename... Params>
+cudaError_t allow_dynamic_smem(void (*kernel)(Params...), size_t smem, SmemAllowance &rec) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (rec.bytes[dev].load(std::memory_order_acquire) >= (int)smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int cur = rec.bytes[dev].load(std::memory_order_relaxed);
+    while (cur < (int)smem && !rec.bytes[dev].compare_exchange_weak(cur, (int)smem)) {
+    }
+    return cudaSuccess;
 }
 
 // Launches `kernel` on `stream` with programmatic stream serialization, so that its

@@ -1,546 +1,15 @@
-// paged_decode.cu -- decode attention over a block-paged KV cache (sm_103a), and the
-// log-sum-exp merge of split contexts.
-//
-// Method ("vLLM推理引擎架构PagedAttention机制与高吞吐推理", lpnh.cn, §2.3 PagedAttention
-// Kernel): for each sequence, find each token's KV block through block_tables, score
-// the query against the keys inside the block, and accumulate across blocks.  The
-// accumulation across blocks is an online softmax in fp32 (running max m, running sum
-// l, rescaled output o); parts of one context computed by different thread blocks are
-// merged with their log-sum-exp weights.
-//
-// GB300 design
-//  * Work is the flat list of (sequence, KV-head tile, 16-token block) units.  A
-//    persistent grid of one CTA per SM takes an equal contiguous share of it (+-1
-//    block), so a 32k context and a 500-token one cost the same per block and no SM
-//    idles in a tail.  A CTA's share can start or end inside a sequence: those parts go
-//    to a workspace slot and the merge kernel combines them.
-//  * A CTA covers all KV heads of its tile (8 for Llama-70B shapes), so each pool block
-//    it touches is read as whole 16-token x 2 KiB rows: one producer warp streams K and
-//    V of each block with TMA (128-byte swizzled, evict-first) into a ring of shared
-//    memory stages guarded by mbarriers; the block id comes from the block table.
-//  * One consumer warp per (KV head, 16 query heads): GQA puts the group's query heads
-//    on the 16 rows of an m16n8k16 bf16 tensor-core MMA, so one K/V read from shared
-//    memory serves the whole group.  S = Q K^T and O += P V use ldmatrix fragments from
-//    the swizzled tiles; the S accumulator becomes the P operand without a shuffle.
-//  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
-//    reports PKV_DEVERR_TIMEOUT instead of hanging.
-#include "attn_block.cuh"
-#include "fp8_block.cuh"
-#include "kv_quant.cuh"
-#include "merge.cuh"
-#include "paged_decode.cuh"
-#include "pkv_split.cuh"
+// paged_decode.cu -- the decode attention kernel over a block-paged KV cache (sm_103a)
+// and its launcher; the CTA body is decode_cta.cuh, the merge of split contexts
+// merge.cuh.
+#include "decode_cta.cuh"
 
 namespace pkv {
 
-namespace {
-
-// The kernel's unit of work is a 16-token slice of a sequence ("unit"); a pool block of
-// block_size tokens holds block_size / 16 units (block sizes 16, 32, 64) or half of one
-// (block size 8: a unit's two halves come from two pool blocks).
-constexpr int kBS = 16;
-
-// Blocks of KV the work item (virtual sequence) v contributes.
-__device__ __forceinline__ int32_t item_blocks(const DecodeArgs &a, int v, bool report) {
-    const int s = v / a.head_tiles;
-    int32_t ctx = a.context_lens[s];
-    if (a.query_start_loc) {
-        const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-        if (q0 < 0 || q1 < q0 || q1 > a.total_q) {
-            if (report) flag_error(a.err, PKV_DEVERR_QUERY_LEN);
-            return 0;
-        }
-        if (q1 - q0 != 1) return 0;  // a prefill chunk (other kernel) or no rows
-        if (ctx < 1) {
-            if (report) flag_error(a.err, PKV_DEVERR_QUERY_LEN);
-            return 0;
-        }
-    }
-    if (ctx < 0 || (int64_t)ctx > (int64_t)a.max_blocks_per_seq * a.block_size) {
-        if (report) flag_error(a.err, PKV_DEVERR_CONTEXT_LEN);
-        return 0;
-    }
-    return (ctx + kBS - 1) / kBS;
-}
-
-// Exclusive prefix sum of item_blocks over all items, into pre[0..V] (pre[V] = total).
-__device__ void build_prefix(const DecodeArgs &a, int V, int32_t *pre, int32_t *scan_tmp) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int per = (V + nt - 1) / nt;
-    const int beg = min(V, tid * per), end = min(V, beg + per);
-    int32_t local = 0;
-    for (int v = beg; v < end; ++v) local += item_blocks(a, v, blockIdx.x == 0);
-    // inclusive warp scan
-    const int lane = tid & 31, warp = tid >> 5;
-    int32_t x = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) scan_tmp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = (nt + 31) >> 5;
-        int32_t w = lane < nw ? scan_tmp[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < nw) scan_tmp[lane] = w;  // inclusive warp totals
-    }
-    __syncthreads();
-    int32_t run = x - local + (warp > 0 ? scan_tmp[warp - 1] : 0);
-    for (int v = beg; v < end; ++v) {
-        pre[v] = run;
-        run += item_blocks(a, v, false);
-    }
-    if (tid == nt - 1) pre[V] = run;
-    __syncthreads();
-}
-
-// Largest v in [0, V) with pre[v] <= f, for 0 <= f < pre[V].
-__device__ __forceinline__ int find_item(const int32_t *pre, int V, int64_t f) {
-    int lo = 0, hi = V;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pre[mid] <= f) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-}  // namespace
-
-// CTA 0: one merge job per boundary between CTA shares (the item split there, when that
-// is its first split), and zero rows for decode rows whose context is empty.
-template <int D>
-__device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pre, int V, int64_t T,
-                                          int ge) {
-    const int rows = a.heads_per_cta * a.group;
-    for (int b = threadIdx.x; b < a.grid; b += blockDim.x) {
-        MergeJob j;
-        no_job(j);
-        if (T > 0 && b < ge - 1) {
-            const int64_t f = share_begin(b + 1, T, ge);
-            const int v = find_item(pre, V, f);
-            const int64_t item_beg = pre[v];
-            if (item_beg != f && item_beg >= share_begin(b, T, ge)) {
-                const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
-                j.item_begin = item_beg;
-                j.total_units = T;
-                j.out_row0 = a.query_start_loc ? a.query_start_loc[s] : s;
-                j.c0 = b;
-                j.c1 = share_owner(pre[v + 1] - 1, T, ge);
-                j.ge = ge;
-                j.rows = rows;
-                j.rows_per_token = rows;
-                j.head0 = ht * rows;
-            }
-        }
-        a.ws_jobs[b] = j;
-    }
-    const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int v = w; v < V; v += nw) {  // one warp per empty item
-        if (pre[v] != pre[v + 1]) continue;
-        const int s = v / a.head_tiles, ht = v - s * a.head_tiles;
-        int64_t qrow = s;
-        if (a.query_start_loc) {
-            const int32_t q0 = a.query_start_loc[s], q1 = a.query_start_loc[s + 1];
-            if (q1 - q0 != 1 || q0 < 0 || q1 > a.total_q) continue;
-            qrow = q0;
-        }
-        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)ht * rows) * D;
-        for (int i = lane; i < rows * D / 2; i += 32) reinterpret_cast<uint32_t *>(orow)[i] = 0u;
-    }
-}
-
-// FP8: the cache holds e4m3 codes (head_dim 128 only); see fp8_block.cuh.  NTH: n-tiles of
-// query heads per consumer warp in the FP8 form (1: a KV head has at most 8 query heads).
 template <int D, bool FP8, int NTH>
 __global__ void __launch_bounds__(288, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
-    static_assert(!FP8 || D == 128, "the FP8 cache path is built for head_dim 128");
-    constexpr int KSTEPS = D / 16;         // k-steps of the QK^T MMA
-    constexpr int NT_D = D / 8;            // n-tiles of the PV MMA
-    constexpr int DCH = FP8 ? 1 : D / 64;  // TMA boxes per block row (128 bytes each)
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int HT = a.heads_per_cta;
-    const int NST = a.num_stages;
-    const uint32_t stage_bytes = (uint32_t)HT * D * kBS * (FP8 ? 1 : 2);
-    const uint32_t chunk_stride = (uint32_t)HT * kBS * 128;  // between 64-column sub-tiles
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NST * stage_bytes);
-    uint64_t *empty = full + NST;
-    int32_t *scan_tmp = reinterpret_cast<int32_t *>(empty + NST);  // 32 ints
-    volatile int *abort_flag = scan_tmp + 32;
-    int32_t *pre = scan_tmp + 36;
-
-    const int V = a.num_seqs * a.head_tiles;
-    const int ncw = HT * a.warps_per_head;  // consumer warps
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], ncw);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (threadIdx.x == 32 * ncw) {
-        tma_prefetch_desc(&k_map);
-        tma_prefetch_desc(&v_map);
-    }
-    // Everything above overlaps the previous kernel; from here on we read its output.
-    pdl_wait();
-    pdl_trigger();
-    build_prefix(a, V, pre, scan_tmp);  // ends with __syncthreads
-    const int64_t T = pre[V];
-    const int ge = split_ctas(T, a.grid, a.min_blocks_per_cta);
-    if (blockIdx.x == 0) write_jobs_and_empty_rows<D>(a, pre, V, T, ge);
-    if ((int)blockIdx.x >= ge || T == 0) return;
-    const int c = blockIdx.x;
-    const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
-
-    if (warp == ncw) {
-        // ------------------------------ producer ------------------------------
-        const uint64_t policy = l2_policy_evict_first();
-        uint32_t stage = 0, phase = 0;
-        uint32_t issued = 0;
-        bool ok = true;
-        const int bsz = a.block_size;
-        auto checked = [&](int id) {
-            if (id < 0 || (int64_t)id >= a.num_blocks) {
-                flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                return -1;  // TMA fills the out-of-range box with zeros
-            }
-            return id;
-        };
-        const int Hkv = a.num_heads / a.group;
-        for (int64_t f0 = lo; f0 < hi && ok; f0 += 32) {
-            const int64_t f = f0 + lane;
-            int bid = -1, bid2 = -1, ht = 0, tok0 = 0;
-            int64_t wslot = -1;  // fused KV write: slot of the new token if this is its unit
-            int wseq = 0;
-            if (f < hi) {
-                const int v = find_item(pre, V, f);
-                const int s = v / a.head_tiles;
-                ht = v - s * a.head_tiles;
-                const int lb = (int)(f - pre[v]);  // unit inside the sequence
-                const int32_t *row = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
-                if (a.k_new && f == pre[v + 1] - 1) {
-                    const int p = a.context_lens[s] - 1;  // the new token's position
-                    const int nb = checked(row[p / bsz]);
-                    if (nb >= 0) {
-                        wslot = (int64_t)nb * bsz + p % bsz;
-                        wseq = s;
-                        // pull the new rows into L2 now: the copy below runs when the unit
-                        // comes up, up to 32 units later
-                        const int64_t src = ((int64_t)s * Hkv + (int64_t)ht * HT) * D * 2;
-                        const char *kp = static_cast<const char *>(a.k_new) + src;
-                        const char *vp = static_cast<const char *>(a.v_new) + src;
-                        for (int off = 0; off < HT * D * 2; off += 128) {
-                            asm volatile("prefetch.global.L2 [%0];" ::"l"(kp + off));
-                            asm volatile("prefetch.global.L2 [%0];" ::"l"(vp + off));
-                        }
-                    }
-                }
-                if (bsz >= kBS) {
-                    const int r = bsz / kBS;
-                    bid = checked(row[lb / r]);
-                    tok0 = (lb % r) * kBS;
-                } else {  // 8-token blocks: the unit's second half exists only inside the context
-                    bid = checked(row[2 * lb]);
-                    if (2 * lb + 1 < (a.context_lens[s] + bsz - 1) / bsz) bid2 = checked(row[2 * lb + 1]);
-                }
-            }
-            const int n = (int)min64(32, hi - f0);
-            for (int j = 0; j < n; ++j) {
-                const int b = __shfl_sync(0xffffffffu, bid, j);
-                const int b2 = __shfl_sync(0xffffffffu, bid2, j);
-                const int t = __shfl_sync(0xffffffffu, ht, j);
-                const int tk = __shfl_sync(0xffffffffu, tok0, j);
-                const int64_t ws = __shfl_sync(0xffffffffu, wslot, j);
-                if (ws >= 0) {
-                    // The unit holds its sequence's new token: store the token's K and V rows
-                    // for this item's heads (the whole warp), then order those stores before
-                    // the TMA reads of the unit (async proxy) issued below.
-                    const int sj = __shfl_sync(0xffffffffu, wseq, j);
-                    const int64_t dst_off = ws * Hkv + (int64_t)t * HT;   // in head rows
-                    const int64_t src_off = (int64_t)sj * Hkv + (int64_t)t * HT;
-                    if constexpr (FP8) {
-                        constexpr int V16 = D / 16;  // 16-code vectors per head row
-                        const uint4 *ks = reinterpret_cast<const uint4 *>(a.k_new) + src_off * (D / 8);
-                        const uint4 *vs = reinterpret_cast<const uint4 *>(a.v_new) + src_off * (D / 8);
-                        uint4 *kd = reinterpret_cast<uint4 *>(a.k_cache_w) + dst_off * V16;
-                        uint4 *vd = reinterpret_cast<uint4 *>(a.v_cache_w) + dst_off * V16;
-                        for (int i = lane; i < HT * V16; i += 32) {
-                            const uint4 k0 = ks[2 * i], k1 = ks[2 * i + 1];
-                            const uint4 v0 = vs[2 * i], v1 = vs[2 * i + 1];
-                            kd[i] = make_uint4(e4m3x4_of(k0.x, k0.y, a.k_scale_q), e4m3x4_of(k0.z, k0.w, a.k_scale_q),
-                                               e4m3x4_of(k1.x, k1.y, a.k_scale_q), e4m3x4_of(k1.z, k1.w, a.k_scale_q));
-                            vd[i] = make_uint4(e4m3x4_of(v0.x, v0.y, a.v_scale_q), e4m3x4_of(v0.z, v0.w, a.v_scale_q),
-                                               e4m3x4_of(v1.x, v1.y, a.v_scale_q), e4m3x4_of(v1.z, v1.w, a.v_scale_q));
-                        }
-                    } else {
-                        constexpr int V8 = D / 8;  // 16-byte vectors per head row
-                        const uint4 *ks = reinterpret_cast<const uint4 *>(a.k_new) + src_off * V8;
-                        const uint4 *vs = reinterpret_cast<const uint4 *>(a.v_new) + src_off * V8;
-                        uint4 *kd = reinterpret_cast<uint4 *>(a.k_cache_w) + dst_off * V8;
-                        uint4 *vd = reinterpret_cast<uint4 *>(a.v_cache_w) + dst_off * V8;
-                        for (int i = lane; i < HT * V8; i += 32) {
-                            kd[i] = ks[i];
-                            vd[i] = vs[i];
-                        }
-                    }
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    __syncwarp();
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&full[stage], stage_bytes);
-                        uint8_t *dst = smem + (size_t)stage * stage_bytes;
-                        const CUtensorMap *map = kv == 0 ? &k_map : &v_map;
-                        if (bsz >= kBS) {
-#pragma unroll
-                            for (int dc = 0; dc < DCH; ++dc)
-                                tma_load_5d(dst + dc * chunk_stride, map, &full[stage], 0, tk, t * HT,
-                                            dc, b, policy);
-                        } else {
-                            // one 8-token box per head and half: each head's 16 rows stay
-                            // contiguous (the swizzle follows the shared-memory address)
-                            for (int dc = 0; dc < DCH; ++dc)
-                                for (int h = 0; h < HT; ++h)
-                                    for (int half = 0; half < 2; ++half)
-                                        tma_load_5d(dst + dc * chunk_stride + h * (kBS * 128) + half * (8 * 128),
-                                                    map, &full[stage], 0, 0, t * HT + h, dc, half ? b2 : b,
-                                                    policy);
-                        }
-                        ++issued;
-                        if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-        }
-        if (!ok && lane == 0) {
-            flag_error(a.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            // Let the copies already issued land before the CTA's shared memory goes away.
-            const uint32_t pending = minu32(issued, (uint32_t)NST);
-            uint32_t st = stage, ph = phase;
-            for (uint32_t i = 0; i < pending; ++i) {
-                if (st == 0) { st = NST; ph ^= 1; }
-                --st;
-                mbar_wait(&full[st], ph, nullptr);
-            }
-        }
-        return;
-    }
-    if (warp > ncw) return;
-
-    // -------------------------------- consumers --------------------------------
-    const int hh = warp / a.warps_per_head;                 // KV head inside the tile
-    const int r0 = (warp - hh * a.warps_per_head) * 16;     // first query row of the group
-    const int g_row = lane >> 2, q4 = lane & 3;
-    const int group = a.group;
-    const uint32_t smem_base = smem_u32(smem);
-    const float sl2 = a.scale_log2;
-
-    uint32_t stage = 0, phase = 0;
-    int64_t f = lo;
-    RowState<D> st;  // bf16 cache: heads on the MMA's M
-    HeadState<NTH> hs;  // FP8 cache: heads on the MMA's N (fp8_block.cuh)
-    while (f < hi) {
-        const int v = find_item(pre, V, f);
-        const int s = v / a.head_tiles;
-        const int ht = v - s * a.head_tiles;
-        const int64_t item_beg = pre[v], item_end = pre[v + 1];
-        const int64_t seg_end = min64(hi, item_end);
-        const int ctx = a.context_lens[s];
-        const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
-        const int kvh = ht * HT + hh;
-        const int rows_valid = min(16, group - r0);  // query heads this warp owns
-
-        // Q fragments (A operand, rows = query heads of the group).
-        uint32_t qa[KSTEPS][4];
-        if constexpr (FP8) {
-            load_q_fp8order(qa, a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D, rows_valid, lane);
-        } else {
-            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
-                a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D);
-            const bool v0 = g_row < rows_valid, v1 = g_row + 8 < rows_valid;
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                const int col = ks * 16 + 2 * q4;
-                qa[ks][0] = v0 ? __ldg(q0 + (g_row * D + col) / 2) : 0u;
-                qa[ks][1] = v1 ? __ldg(q0 + ((g_row + 8) * D + col) / 2) : 0u;
-                qa[ks][2] = v0 ? __ldg(q0 + (g_row * D + col + 8) / 2) : 0u;
-                qa[ks][3] = v1 ? __ldg(q0 + ((g_row + 8) * D + col + 8) / 2) : 0u;
-            }
-        }
-        if constexpr (FP8) hs.reset();
-        else st.reset();
-
-        bool ok = true;
-        for (; f < seg_end; ++f) {
-            const int lb = (int)(f - item_beg);
-            const int valid = min(kBS, ctx - lb * kBS);
-            // ---- S = Q K^T over the block's 16 tokens ----
-            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            float sacc[2][4];
-            if constexpr (FP8)
-                qk_block_fp8t<NTH>(reinterpret_cast<float(&)[NTH][4]>(sacc), qa,
-                                   smem_base + stage * stage_bytes + hh * (kBS * 128), lane);
-            else qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-
-            // ---- scale, mask the block's tail, online softmax (base 2) ----
-            const bool tail = valid < kBS;  // only a sequence's last block
-            if constexpr (FP8) {
-                // S^T: tokens g (entries 0, 1) and g + 8 (entries 2, 3) of each n-tile
-                const bool in0 = !tail || g_row < valid, in1 = !tail || g_row + 8 < valid;
-                uint32_t pb[NTH][2];
-#pragma unroll
-                for (int nt = 0; nt < NTH; ++nt) {
-                    sacc[nt][0] = in0 ? sacc[nt][0] * sl2 : -INFINITY;
-                    sacc[nt][1] = in0 ? sacc[nt][1] * sl2 : -INFINITY;
-                    sacc[nt][2] = in1 ? sacc[nt][2] * sl2 : -INFINITY;
-                    sacc[nt][3] = in1 ? sacc[nt][3] * sl2 : -INFINITY;
-                    softmax_update_t(hs, nt, sacc[nt], pb[nt]);
-                }
-                // ---- O^T += V^T P^T ----
-                if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-                const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-                if (tail) pv_block_fp8t<true>(hs, pb, vtile, valid, lane);
-                else pv_block_fp8t<false>(hs, pb, vtile, valid, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-                continue;
-            }
-            if (tail) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool in = nt * 8 + 2 * q4 + e < valid;
-                        sacc[nt][e] = in ? sacc[nt][e] * sl2 : -INFINITY;
-                        sacc[nt][2 + e] = in ? sacc[nt][2 + e] * sl2 : -INFINITY;
-                    }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sacc[0][i] *= sl2;
-                    sacc[1][i] *= sl2;
-                }
-            }
-            uint32_t pa[4];
-            softmax_update<D>(st, sacc, pa);
-
-            // ---- O += P V ----
-            if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-            const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-            if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
-            else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-        }
-        if (!ok) {
-            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            return;
-        }
-
-        // ---- finish this item's part ----
-        const int64_t seg_beg = max64(lo, item_beg);
-        const bool whole = seg_beg == item_beg && seg_end == item_end;
-        if constexpr (FP8) {
-            // lane (g, t) holds dims 16g .. 16g + 15 of heads 8nt + 2t + e: dim 16g + 2mt in
-            // o[nt][mt][e], 16g + 2mt + 1 in o[nt][mt][2 + e]; the V scale comes in here
-            finish_sums_t(hs);
-            const float vs = a.v_scale;
-            const int rows = HT * group;
-            const int row0 = hh * group + r0;  // row inside the item
-            const int slot = whole ? 0 : part_slot(c, item_beg, T, ge);
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int hd = 8 * nt + 2 * q4 + e;  // head inside the warp's 16
-                    if (hd >= rows_valid) continue;
-                    if (whole) {
-                        const float inv = vs / hs.l[nt][e];
-                        uint32_t p[8];
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt)
-                            p[mt] = pack_bf16x2(hs.o[nt][mt][e] * inv, hs.o[nt][mt][2 + e] * inv);
-                        uint4 *orow = reinterpret_cast<uint4 *>(
-                            a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0 + hd) * D + 16 * g_row);
-                        orow[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        orow[1] = make_uint4(p[4], p[5], p[6], p[7]);
-                    } else {
-                        float4 *ob = reinterpret_cast<float4 *>(a.ws_o + ((int64_t)slot * rows + row0 + hd) * D +
-                                                                16 * g_row);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ob[k] = make_float4(hs.o[nt][2 * k][e] * vs, hs.o[nt][2 * k][2 + e] * vs,
-                                                hs.o[nt][2 * k + 1][e] * vs, hs.o[nt][2 * k + 1][2 + e] * vs);
-                        if (g_row == 0)
-                            a.ws_ml[(int64_t)slot * rows + row0 + hd] = make_float2(hs.m[nt][e], hs.l[nt][e]);
-                    }
-                }
-            f = seg_end;
-            continue;
-        }
-        finish_sums<D>(st);
-        if (whole) {
-            const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
-            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (g_row < rows_valid)
-                    *reinterpret_cast<uint32_t *>(orow + g_row * D + col) =
-                        pack_bf16x2(st.o[n][0] * inv0, st.o[n][1] * inv0);
-                if (g_row + 8 < rows_valid)
-                    *reinterpret_cast<uint32_t *>(orow + (g_row + 8) * D + col) =
-                        pack_bf16x2(st.o[n][2] * inv1, st.o[n][3] * inv1);
-            }
-        } else {
-            const int slot = part_slot(c, item_beg, T, ge);
-            const int rows = HT * group;
-            const int row0 = hh * group + r0;  // row inside the item
-            float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D;
-            float2 *mlb = a.ws_ml + (int64_t)slot * rows + row0;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (g_row < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + g_row * D + col) = make_float2(st.o[n][0], st.o[n][1]);
-                if (g_row + 8 < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + (g_row + 8) * D + col) = make_float2(st.o[n][2], st.o[n][3]);
-            }
-            if (q4 == 0) {
-                if (g_row < rows_valid) mlb[g_row] = make_float2(st.m0, st.l0);
-                if (g_row + 8 < rows_valid) mlb[g_row + 8] = make_float2(st.m1, st.l1);
-            }
-        }
-        f = seg_end;
-    }
+    decode_cta<D, FP8, NTH>(k_map, v_map, a, (int)blockIdx.x, a.grid, true);
 }
 
 template __global__ void paged_decode_kernel<64, false, 1>(const __grid_constant__ CUtensorMap,
@@ -563,8 +32,8 @@ template <int D, bool FP8, int NTH>
 static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &v_map,
                                    const DecodeArgs &a, size_t smem, cudaStream_t stream) {
     const int ncw = a.heads_per_cta * a.warps_per_head;
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, FP8, NTH>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static SmemAllowance allowed;
+    cudaError_t e = allow_dynamic_smem(paged_decode_kernel<D, FP8, NTH>, smem, allowed);
     if (e != cudaSuccess) return e;
     e = launch_pdl(paged_decode_kernel<D, FP8, NTH>, dim3(a.grid), dim3((ncw + 1) * 32), smem, stream, k_map,
                    v_map, a);

@@ -34,6 +34,7 @@ struct DecodeArgs {
     float2 *ws_ml;       // [2 * grid][heads_per_cta * group]  (running max, sum)
     float *ws_o;         // [2 * grid][heads_per_cta * group][head_dim]
     int *err;            // device error word
+    uint64_t wait_ns;    // limit of a pipeline wait (see pkv_common.cuh)
     // Fused KV write (null k_new: none): before a sequence's last unit is read, its new
     // token's rows k_new[s], v_new[s] ([num_seqs][Hkv][D] bf16) are stored at position
     // context_lens[s] - 1 of k_cache_w / v_cache_w (quantised with k_scale_q / v_scale_q for

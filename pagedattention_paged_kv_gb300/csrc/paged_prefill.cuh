@@ -1,11 +1,16 @@
-// paged_prefill.cuh -- arguments, plan and launcher of the chunked-prefill kernel
-// (paged_prefill.cu): attention for every sequence of a varlen batch with q_len >= 2.
+// paged_prefill.cuh -- arguments and plan of the chunked-prefill CTAs (prefill_cta.cuh,
+// paged_prefill.cu): attention for every sequence of a varlen batch with q_len >= 2.
 #pragma once
 
 #include "merge.cuh"
 #include "pkv_common.cuh"
 
 namespace pkv {
+
+// 12 warps: warpgroup 0 = TMA producer, tcgen05 issuer and two warps that convert FP8
+// operands (idle with a bf16 cache); warpgroups 1 and 2 = softmax of the tile's two
+// halves.  Launched at 168 registers a thread, the most 12 warps may hold.
+constexpr int kPrefillThreads = 384;
 
 // A work item ("tile") is tokens_per_tile consecutive query tokens of one sequence
 // together with all `group` query heads of one KV head: rows r = token * group + head,
@@ -33,6 +38,7 @@ struct PrefillArgs {
     float *ws_o;             // [2 * grid][rows][head_dim]
     int max_seqs;
     int *err;
+    uint64_t wait_ns;  // limit of a pipeline wait (see pkv_common.cuh)
     // FP8 cache (the FP8 kernel): e4m3 K/V land in a ring of num_stages8 byte stages and are
     // widened to fp16 into the num_stages-slot operand ring; V elements mean code x v_scale
     // (the K scale is folded into scale_log2).
@@ -50,8 +56,5 @@ struct PrefillPlan {
 // PKV_ERR_UNSUPPORTED.
 int plan_prefill(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms,
                  int smem_optin, PrefillPlan *p, bool fp8 = false);
-cudaError_t launch_paged_prefill(int head_dim, bool fp8, const CUtensorMap &q_map, const CUtensorMap &k_map,
-                                 const CUtensorMap &v_map, const PrefillArgs &a,
-                                 const PrefillPlan &p, cudaStream_t stream);
 
 }  // namespace pkv

@@ -12,8 +12,15 @@
 
 namespace pkv {
 
-// Every mbarrier wait gives up after this long (ns of %globaltimer) and reports
-// PKV_DEVERR_TIMEOUT instead of spinning forever.
+// Tokens of a work unit: a 16-token slice of a sequence's keys (one pool block at the
+// default block size).
+constexpr int kBS = 16;
+
+// A pipeline wait (a consumer waiting for data, a producer for a free stage) gives up
+// after the launch's limit (DecodeArgs / PrefillArgs::wait_ns, default kWaitTimeoutNs,
+// settable with pkv_set_wait_limit_ns) and reports PKV_DEVERR_TIMEOUT instead of spinning
+// forever.  A wait for the CTA's own copies or MMAs already in flight -- they always
+// complete -- keeps the long limit, so a CTA never exits with them outstanding.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -63,16 +70,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns false
-// (having waited at most kWaitTimeoutNs, or less if *abort becomes non-zero) when
-// the phase did not complete; the caller then stops its pipeline.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+// (having waited at most limit_ns, or less if *abort becomes non-zero) when the phase
+// did not complete; the caller then stops its pipeline.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort_flag && *abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

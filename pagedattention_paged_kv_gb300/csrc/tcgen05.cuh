@@ -138,16 +138,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Per-warp register budget changes (all four warps of a warpgroup execute the same one).
-template <int N>
-__device__ __forceinline__ void reg_alloc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void reg_dealloc() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // Placed after tmem_wait_ld: the registers a tcgen05.ld filled pass through this empty
 // volatile statement, so no use of them can be scheduled above the wait.
 __device__ __forceinline__ void reg_order32(uint32_t (&r)[32]) {

@@ -38,13 +38,21 @@ def test_skewed_long_context_decode():
     _check_step(W.skewed_decode())
 
 
-def test_mixed_varlen_full_size_sampled_chunk_rows():
-    b = W.mixed_varlen()
-    mask = np.zeros(b.q.shape[0], np.uint8)
-    chunk_rows = np.r_[0, 1, 2, 15, 16, 17, 31, 32, np.arange(47, 512, 37), 510, 511]
-    mask[chunk_rows] = 1
-    mask[512:] = 1            # every decode row
-    _check_step(b, row_mask=mask)
+def test_mixed_varlen_full_size_every_row():
+    # workload 4 in one varlen call: the 512-row chunk behind its 16,384-token prefix and the
+    # 127 decodes, every output row against the oracle (decode and prefill CTAs of one launch)
+    _check_step(W.mixed_varlen())
+
+
+@pytest.mark.parametrize("chunk_len,chunk_start,num_decodes", [
+    (16, 0, 127),        # almost all decode work: the grid gives the chunk one or a few CTAs
+    (512, 16384, 1),     # almost all prefill work: one decode CTA
+    (512, 4096, 300),    # more sequences than SMs, both sides split
+])
+def test_mixed_varlen_split_extremes(chunk_len, chunk_start, num_decodes):
+    b = W.mixed_varlen(seed=4100 + num_decodes, chunk_start=chunk_start, chunk_len=chunk_len,
+                       num_decodes=num_decodes)
+    _check_step(b)
 
 
 # ---- shapes and edge cases ----------------------------------------------------------
