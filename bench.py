@@ -68,6 +68,9 @@ def parse():
     p.add_argument("--e2e-copy", choices=["sm", "engine"], default="sm",
                    help="e2e host<->device transfers: the library's SM copies (pkv.copy_to_device / "
                         "copy_to_host, pinned host memory read and written by the SMs) or torch's copy-engine copies")
+    p.add_argument("--part", choices=["all", "chunk", "decodes"], default="all",
+                   help="varlen workloads: time the step on its prefill chunks only or its decode rows "
+                        "only (the same batch restricted to those sequences)")
     p.add_argument("--separate-kv-write", action="store_true",
                    help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
@@ -241,12 +244,13 @@ def kernel_source_sha(files):
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ("paged_decode.cu", "paged_decode.cuh", "attn_block.cuh", "fp8_block.cuh", "pkv_common.cuh",
-                  "pkv_split.cuh", "merge.cuh")
+DECODE_SOURCES = ("api.cu", "paged_decode.cu", "paged_decode.cuh", "decode_cta.cuh", "attn_block.cuh",
+                  "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
 
 
-PREFILL_SOURCES = ("paged_prefill.cu", "paged_prefill.cuh", "tcgen05.cuh", "fp32x2.cuh", "attn_block.cuh", "fp8_block.cuh",
-                   "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
+VARLEN_SOURCES = ("api.cu", "paged_varlen.cu", "paged_varlen.cuh", "prefill_cta.cuh", "paged_prefill.cu",
+                  "paged_prefill.cuh", "decode_cta.cuh", "paged_decode.cuh", "tcgen05.cuh", "fp32x2.cuh",
+                  "attn_block.cuh", "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
 
 
 def recorded_traffic(name, sources, config):
@@ -494,6 +498,13 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     b = make_batch(args.config, seed, args.block_size)
+    if args.part != "all":
+        if b.query_start_loc is None:
+            raise SystemExit("--part applies to the varlen workloads")
+        from pagedattention_paged_kv_gb300 import workloads as W
+        ql = b.q_lens
+        b = W.select_seqs(b, np.nonzero(ql >= 2 if args.part == "chunk" else ql == 1)[0])
+        name = f"{name} ({args.part} only)"
     varlen = b.query_start_loc is not None
     total_bytes, attn_bytes = algorithmic_bytes(b)
     S, Hq, d = b.num_seqs, b.num_heads, b.head_dim
@@ -710,7 +721,7 @@ def main():
 
     # ---- varlen only: the chunk alone and the decodes alone ----
     parts = None
-    if varlen:
+    if varlen and args.part == "all":
         parts = varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, args.config)
 
     if rank != 0:
@@ -747,8 +758,19 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if not varlen:
+    if varlen and args.part == "chunk":
+        fl = chunk_flops(b.context_lens, b.q_lens, d, Hq)
+        tf = fl / (t_attn * 1e-3) / 1e12
+        traffic = recorded_traffic("chunk_fp8" if fp8 else "chunk", VARLEN_SOURCES, args.config)
+        line["roofline"] = {"bound": "tensor", "kernel": "paged_varlen_kernel (prefill CTAs; + merges, timed together)",
+                            "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                            "peak_source": "measured bf16_tflops (burst cuBLAS)",
+                            "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                            "algorithmic_flops": fl}
+    elif not varlen or args.part == "decodes":
         traffic = recorded_traffic("decode_fp8" if fp8 else "decode", DECODE_SOURCES, args.config)
+        if varlen:
+            traffic = None  # recorded for the decode-step launch, not for this batch
         achieved = attn_bytes / (t_attn * 1e-3) / 1e9
         line["roofline"] = {
             "bound": "hbm", "kernel": "paged_decode_kernel (+ merge_parts_kernel, timed together)",
@@ -756,7 +778,7 @@ def main():
             "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
             "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
             "algorithmic_bytes": attn_bytes}
-    else:
+    elif parts is not None:
         line.update(parts)
         overlap_figures(line)
     if not args.no_cpu_baseline:
@@ -814,7 +836,7 @@ def varlen_parts(b, pkv, torch, dev, kc, vc, l2_flush, hbm_peak, tc_peak, config
             tf = fl / (t * 1e-3) / 1e12
             res["chunk_us"] = t * 1e3
             res["chunk_tflops"] = tf
-            traffic = recorded_traffic("prefill_fp8" if fp8 else "prefill", PREFILL_SOURCES, config)
+            traffic = recorded_traffic("chunk_fp8" if fp8 else "chunk", VARLEN_SOURCES, config)
             res["roofline"] = {"bound": "tensor",
                                "kernel": "paged_varlen_kernel on a chunk-only batch (its prefill CTAs; "
                                          "+ merges, timed together)",

@@ -174,6 +174,30 @@ def make_batch(name: str, *, context_lens, q_lens, num_heads: int, num_kv_heads:
                       meta={"seed": seed})
 
 
+def select_seqs(b: PagedBatch, seqs) -> PagedBatch:
+    """The same step restricted to sequences `seqs` (same pool; their block-table rows,
+    context lengths, query rows and new K/V rows, renumbered 0..len(seqs)-1)."""
+    import dataclasses
+    seqs = np.asarray(seqs, dtype=np.int64)
+    ql = b.q_lens
+    qsl = b.query_start_loc if b.query_start_loc is not None else np.arange(b.num_seqs + 1)
+    rows = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seqs]) if len(seqs) else np.zeros(0, np.int64)
+    new_of_old = np.full(b.num_seqs, -1, np.int64)
+    new_of_old[seqs] = np.arange(len(seqs))
+    keep = np.isin(b.new_token_seq, seqs)
+    new_qsl = None
+    if b.query_start_loc is not None:
+        new_qsl = np.concatenate([[0], np.cumsum(ql[seqs])]).astype(np.int32)
+    return dataclasses.replace(
+        b, q=np.ascontiguousarray(b.q[rows]), k_new=np.ascontiguousarray(b.k_new[keep]),
+        v_new=np.ascontiguousarray(b.v_new[keep]),
+        new_token_seq=new_of_old[b.new_token_seq[keep]].astype(np.int32),
+        new_token_pos=np.ascontiguousarray(b.new_token_pos[keep]),
+        block_tables=np.ascontiguousarray(b.block_tables[seqs]),
+        context_lens=np.ascontiguousarray(b.context_lens[seqs]), query_start_loc=new_qsl,
+        meta={**b.meta, "selected_seqs": len(seqs)})
+
+
 # ---------------------------------------------------------------------------
 # FP8 pool: the same step with the pool held as e4m3 codes.
 # ---------------------------------------------------------------------------

@@ -123,6 +123,32 @@ def test_varlen_chunks_and_decodes(q_lens, ctx):
     _check_step(b)
 
 
+def _boost_keys(b, seq, lo, hi, factor):
+    """Multiplies the cached K rows of positions [lo, hi) of sequence `seq` by `factor`
+    (in the pool, through the block table), so the scores against them jump."""
+    for pos in range(lo, hi):
+        blk, off = b.block_tables[seq, pos // b.block_size], pos % b.block_size
+        b.k_cache[blk, off] = W.bf16_bits(W.bf16_to_f32(b.k_cache[blk, off]) * np.float32(factor))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("factor", [6.0, 40.0])
+def test_prefill_score_jumps(factor, fp8):
+    # Keys 900..1000 of a 1500-token context score far above the ones before them: x6 moves
+    # the rows' reference maximum by ~10-25 (log2 units), x40 by far more, so the chunked
+    # prefill takes both its deferred reference move and its exact recomputation of a chunk.
+    b = W.make_batch("jumps", context_lens=[1500, 700, 1200], q_lens=[300, 1, 64], num_heads=64,
+                     num_kv_heads=8, head_dim=128, seed=91, varlen=True)
+    _boost_keys(b, 0, 900, 1000, factor)
+    _boost_keys(b, 2, 300, 310, factor)
+    if fp8:
+        # K scale 1: the boosted keys (|x| up to ~200) stay inside e4m3's range (+-448)
+        from test_gpu_fp8 import _check_fp8
+        _check_fp8(W.to_fp8_pool(b, k_scale=1.0))
+    else:
+        _check_step(b)
+
+
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 64), (8, 2, 128), (12, 4, 64), (56, 8, 128)])
 def test_varlen_head_layouts(Hq, Hkv, d):
     b = W.make_batch("varlen_heads", context_lens=[70, 3, 129], q_lens=[37, 1, 129], num_heads=Hq,

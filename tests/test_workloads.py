@@ -92,3 +92,19 @@ def test_fp8_pool_is_the_e4m3_cast_of_value_over_scale():
     assert np.array_equal(f.k_cache, k.numpy()) and np.array_equal(f.v_cache, v.numpy())
     assert f.meta["k_scale"] == 0.5 and f.meta["v_scale"] == 0.25 and f.meta["kv_dtype"] == "fp8_e4m3"
     assert np.array_equal(f.q, b.q) and np.array_equal(f.k_new, b.k_new)
+
+
+def test_select_seqs_keeps_each_sequence_as_it_was():
+    b = W.mixed_varlen(num_decodes=5)
+    for seqs in ([0], [1, 2, 3, 4, 5], [3, 0]):
+        s = W.select_seqs(b, seqs)
+        assert s.num_seqs == len(seqs)
+        assert np.array_equal(s.context_lens, b.context_lens[seqs])
+        assert np.array_equal(s.block_tables, b.block_tables[seqs])
+        assert np.array_equal(s.q_lens, b.q_lens[seqs])
+        assert s.k_cache is b.k_cache and s.v_cache is b.v_cache
+        for i, old in enumerate(seqs):
+            rows = slice(b.query_start_loc[old], b.query_start_loc[old + 1])
+            assert np.array_equal(s.q[s.query_start_loc[i]:s.query_start_loc[i + 1]], b.q[rows])
+            assert np.array_equal(s.k_new[s.new_token_seq == i], b.k_new[b.new_token_seq == old])
+            assert np.array_equal(s.new_token_pos[s.new_token_seq == i], b.new_token_pos[b.new_token_seq == old])
