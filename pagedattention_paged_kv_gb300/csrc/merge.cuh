@@ -8,8 +8,9 @@
 //
 // The main kernel's CTA 0 writes one MergeJob per boundary between neighbouring CTA
 // shares (the item split there, if that boundary is the item's first split); the merge
-// kernel runs one CTA per 16 rows of a job, so a job costs three rounds of global loads
-// (job, (m, l) of its parts, o of its parts) whatever the batch and however many parts.
+// kernel runs one thread per (row, 4 columns) of a job, so a job costs two rounds of global
+// loads (the job; (m, l) and o of up to four parts together) and one more per four parts
+// beyond.
 #pragma once
 
 #include "attn_block.cuh"
@@ -37,7 +38,6 @@ struct MergeArgs {
     int num_heads;
 };
 
-constexpr int kMergeRows = 16;       // rows per CTA; a job gets ceil(slot_rows / 16) CTAs
 constexpr int kMergeMaxParts = 256;  // the grids hold <= 256 CTAs, so an item has <= 256 parts
 
 __device__ __forceinline__ void no_job(MergeJob &j) {
@@ -46,134 +46,75 @@ __device__ __forceinline__ void no_job(MergeJob &j) {
     j.ge = j.rows = j.rows_per_token = j.head0 = 0;
 }
 
-// Three rounds of global loads per CTA (the job; (m, l) of its rows' parts; o of its
-// rows' parts).  The 8 warps split the (row, part) pairs: G = min(8, parts) part groups
-// (a power of two) times 8 / G row groups, so a job split into many parts keeps every warp
-// busy with independent loads and a two-part job still uses all warps.  The part groups'
-// sums are added in group order (bit-reproducible).
+// One thread per (row, 4 columns) of a job; a CTA covers 256 / (D / 4) rows.  After the
+// job (one load), every part's (m, l) and its 4 columns of o are loaded together, kPC
+// parts per round, and combined in registers: o = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M)
+// l_p, with M the running maximum over the rounds.  Two rounds of global loads for up to
+// kPC parts, no shared memory and no CTA barrier.
 template <int D>
 __global__ void __launch_bounds__(256, 4) merge_parts_kernel(const MergeArgs m) {
-    constexpr int D4 = D / 4;
-    __shared__ float s_w[kMergeRows][kMergeMaxParts];  // m_p, then the weight 2^(m_p - M)
-    __shared__ float s_inv[kMergeRows];
-    __shared__ float4 s_acc[kMergeRows][D4];
+    constexpr int CG = D / 4;         // 16-byte column groups of a row
+    constexpr int RPC = 256 / CG;     // rows per CTA
+    constexpr int kPC = 4;            // parts per round of loads
     pdl_wait();
     const MergeJob j = m.jobs[blockIdx.x];
     if (j.c0 < 0) return;
     const int nparts = j.c1 - j.c0 + 1;
-    const int row0 = blockIdx.y * kMergeRows;
-    if (row0 >= j.rows || nparts > kMergeMaxParts) return;
-    const int nrows = min(kMergeRows, j.rows - row0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // (1) warp w: the weights of rows w and w + 8
-    for (int k = warp; k < nrows; k += 8) {
-        const int row = row0 + k;
-        float M = -INFINITY, lv[kMergeMaxParts / 32];
+    const int row = blockIdx.y * RPC + (int)threadIdx.x / CG;
+    if (row >= j.rows || nparts > kMergeMaxParts) return;
+    const int cg = (int)threadIdx.x % CG;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < nparts; p0 += kPC) {
+        float2 ml[kPC];
+        float4 o[kPC];
 #pragma unroll
-        for (int i = 0; i < kMergeMaxParts / 32; ++i) {
-            const int p = lane + 32 * i;
-            lv[i] = 0.f;
-            if (p < nparts) {
-                const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
-                const float2 ml = m.ws_ml[(int64_t)slot * m.slot_rows + row];
-                s_w[k][p] = ml.x;
-                lv[i] = ml.y;
-                M = fmaxf(M, ml.x);
+        for (int q = 0; q < kPC; ++q) {
+            if (p0 + q < nparts) {
+                const int slot = part_slot(j.c0 + p0 + q, j.item_begin, j.total_units, j.ge);
+                const int64_t r = (int64_t)slot * m.slot_rows + row;
+                ml[q] = __ldcg(m.ws_ml + r);
+                o[q] = __ldcg(reinterpret_cast<const float4 *>(m.ws_o + r * D) + cg);
+            } else {
+                ml[q] = make_float2(-INFINITY, 0.f);
+                o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+        float mc = M;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float base = M == -INFINITY ? 0.f : M;  // rows that saw nothing keep weight 0
-        float L = 0.f;
+        for (int q = 0; q < kPC; ++q) mc = fmaxf(mc, ml[q].x);
+        if (mc == -INFINITY) continue;  // nothing seen yet (rows of empty parts keep weight 0)
+        const float a0 = M == -INFINITY ? 0.f : fast_exp2(M - mc);
+        L *= a0;
+        acc.x *= a0;
+        acc.y *= a0;
+        acc.z *= a0;
+        acc.w *= a0;
 #pragma unroll
-        for (int i = 0; i < kMergeMaxParts / 32; ++i) {
-            const int p = lane + 32 * i;
-            if (p < nparts) {
-                const float w = fast_exp2(s_w[k][p] - base);
-                s_w[k][p] = w;
-                L += w * lv[i];
-            }
+        for (int q = 0; q < kPC; ++q) {
+            if (ml[q].x == -INFINITY) continue;
+            const float w = fast_exp2(ml[q].x - mc);
+            L += w * ml[q].y;
+            acc.x += w * o[q].x;
+            acc.y += w * o[q].y;
+            acc.z += w * o[q].z;
+            acc.w += w * o[q].w;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) s_inv[k] = 1.f / L;
+        M = mc;
     }
-    __syncthreads();
-    // (2) warp w = (row group rg, part group pg): rows rg, rg + RG, ...; parts pg, pg + G, ...
-    const int G = nparts >= 8 ? 8 : nparts >= 4 ? 4 : nparts >= 2 ? 2 : 1;
-    const int RG = 8 / G;
-    const int pg = warp % G, rg = warp / G;
-    static_assert(D4 <= 32, "one lane per 4 columns");
-    const int d4 = lane;
-    const bool col = d4 < D4;
-    // rows in passes of 4 per warp (few registers: the CTA then fits next to the tail of
-    // the kernel that produced the parts)
-    for (int r0 = 0; r0 < nrows; r0 += 4 * RG) {
-        float4 acc[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (col) {
-#pragma unroll 2
-            for (int p = pg; p < nparts; p += G) {
-                const int slot = part_slot(j.c0 + p, j.item_begin, j.total_units, j.ge);
-                const float4 *ob =
-                    reinterpret_cast<const float4 *>(m.ws_o + ((int64_t)slot * m.slot_rows + row0) * D);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int k = r0 + rg + i * RG;
-                    if (k < nrows) {
-                        const float w = s_w[k][p];
-                        const float4 ov = ob[k * D4 + d4];
-                        acc[i].x += w * ov.x;
-                        acc[i].y += w * ov.y;
-                        acc[i].z += w * ov.z;
-                        acc[i].w += w * ov.w;
-                    }
-                }
-            }
-        }
-        // (3) add the part groups in order: group 0 stores, groups 1 .. G-1 add in turn
-        // (every thread takes every barrier)
-        for (int g = 0; g < G; ++g) {
-            if (pg == g && col) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int k = r0 + rg + i * RG;
-                    if (k < nrows) {
-                        if (g == 0) {
-                            s_acc[k][d4] = acc[i];
-                        } else {
-                            float4 t = s_acc[k][d4];
-                            t.x += acc[i].x;
-                            t.y += acc[i].y;
-                            t.z += acc[i].z;
-                            t.w += acc[i].w;
-                            s_acc[k][d4] = t;
-                        }
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // (4) one thread per (row, 4 columns): normalise, store bf16
-    for (int idx = threadIdx.x; idx < nrows * D4; idx += blockDim.x) {
-        const int k = idx / D4, d4 = idx - k * D4;
-        const float4 t = s_acc[k][d4];
-        const float inv = s_inv[k];
-        const int row = row0 + k;
-        const int tok = row / j.rows_per_token, hr = row - tok * j.rows_per_token;
-        __nv_bfloat16 *orow = m.out + ((j.out_row0 + tok) * (int64_t)m.num_heads + j.head0 + hr) * D;
-        uint2 packed;
-        packed.x = pack_bf16x2(t.x * inv, t.y * inv);
-        packed.y = pack_bf16x2(t.z * inv, t.w * inv);
-        reinterpret_cast<uint2 *>(orow)[d4] = packed;
-    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int tok = row / j.rows_per_token, hr = row - tok * j.rows_per_token;
+    __nv_bfloat16 *orow = m.out + ((j.out_row0 + tok) * (int64_t)m.num_heads + j.head0 + hr) * D;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2 *>(orow)[cg] = packed;
 }
 
 template <int D>
 cudaError_t launch_merge(const MergeArgs &m, int grid, cudaStream_t stream) {
-    const int ny = (m.slot_rows + kMergeRows - 1) / kMergeRows;
+    constexpr int RPC = 256 / (D / 4);
+    const int ny = (m.slot_rows + RPC - 1) / RPC;
     return launch_pdl(merge_parts_kernel<D>, dim3(grid, ny), dim3(256), 0, stream, m);
 }
 
