@@ -53,12 +53,12 @@ DeviceInfo g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{pkv::kWaitTimeoutNs};
 
 // Measured GB300 rates behind the varlen grid split (paged_varlen.cu).  A decode CTA that
-// shares the GPU with prefill CTAs streams ~70 GB/s of bf16 K/V (~42 GB/s of FP8 codes);
-// alone, a few decode CTAs reach ~90 (~48) GB/s each.  The whole decode saturates near
+// shares the GPU with prefill CTAs streams ~83 GB/s of bf16 K/V (~42 GB/s of FP8 codes);
+// alone, a few decode CTAs reach ~95-105 (~48) GB/s each.  The whole decode saturates near
 // 5.9 TB/s; a prefill CTA sustains ~7.8 TFLOP/s of causal attention.  On the 512-token
-// chunk + 127 decodes step these rates put the split at the measured optimum (36 of 152
-// CTAs decode with a bf16 cache, 32 with an FP8 one).
-constexpr float kDecodeBytesPerUsSm = 70e3f;
+// chunk + 127 decodes step these rates put the split at the measured optimum (32 of 152
+// CTAs decode, with a bf16 or an FP8 cache).
+constexpr float kDecodeBytesPerUsSm = 83e3f;
 constexpr float kDecodeBytesPerUsSmFp8 = 42e3f;
 constexpr float kDecodeBytesPerUsGpu = 5.9e6f;
 constexpr float kPrefillFlopPerUsSm = 7.8e6f;

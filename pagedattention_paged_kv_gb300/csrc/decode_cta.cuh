@@ -18,15 +18,17 @@
 //    it touches is read as whole 16-token x 2 KiB rows: one producer warp streams K and
 //    V of each block with TMA (128-byte swizzled, evict-first) into a ring of shared
 //    memory stages guarded by mbarriers; the block id comes from the block table.
-//  * One consumer warp per (KV head, 16 query heads): GQA puts the group's query heads
-//    on the 16 rows of an m16n8k16 bf16 tensor-core MMA, so one K/V read from shared
-//    memory serves the whole group.  S = Q K^T and O += P V use ldmatrix fragments from
-//    the swizzled tiles; the S accumulator becomes the P operand without a shuffle.
+//  * One consumer warp per (KV head, up to 16 query heads): GQA puts the group's query
+//    heads on the N of m16n8k16 tensor-core MMAs and the block's 16 tokens on M, so one
+//    K/V read from shared memory serves the whole group with no padded rows (8 heads
+//    fill N): S^T = K Q^T and O^T += V^T P^T (bf16t_block.cuh; fp8_block.cuh for an FP8
+//    cache).
 //  * No thread ever waits on another CTA.  Every mbarrier wait is bounded in time and
 //    reports PKV_DEVERR_TIMEOUT instead of hanging.
 #pragma once
 
 #include "attn_block.cuh"
+#include "bf16t_block.cuh"
 #include "fp8_block.cuh"
 #include "kv_quant.cuh"
 #include "merge.cuh"
@@ -161,14 +163,13 @@ __device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pr
 // are written for all a.grid job slots (a.grid >= grid_eff).  `pdl`: wait for the
 // previous kernel here (false when the caller already did).
 // FP8: the cache holds e4m3 codes (head_dim 128 only); see fp8_block.cuh.  NTH: n-tiles of
-// query heads per consumer warp in the FP8 form (1: a KV head has at most 8 query heads).
+// 8 query heads per consumer warp (1: a KV head has at most 8 query heads, else 2).
 template <int D, bool FP8, int NTH>
 __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUtensorMap &v_map,
                                            const DecodeArgs &a, const int cta, const int grid_eff,
                                            const bool pdl) {
     static_assert(!FP8 || D == 128, "the FP8 cache path is built for head_dim 128");
     constexpr int KSTEPS = D / 16;         // k-steps of the QK^T MMA
-    constexpr int NT_D = D / 8;            // n-tiles of the PV MMA
     constexpr int DCH = FP8 ? 1 : D / 64;  // TMA boxes per block row (128 bytes each)
 
     extern __shared__ uint8_t smem_raw[];
@@ -357,8 +358,10 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
     if (warp > ncw) return;
 
     // -------------------------------- consumers --------------------------------
+    // Both caches put the group's query heads on the MMA's N and the block's 16 tokens on
+    // M (S^T = K Q^T, O^T += V^T P^T): bf16t_block.cuh for bf16, fp8_block.cuh for e4m3.
     const int hh = warp / a.warps_per_head;                 // KV head inside the tile
-    const int r0 = (warp - hh * a.warps_per_head) * 16;     // first query row of the group
+    const int r0 = (warp - hh * a.warps_per_head) * 16;     // first query head of the warp
     const int g_row = lane >> 2, q4 = lane & 3;
     const int group = a.group;
     const uint32_t smem_base = smem_u32(smem);
@@ -366,8 +369,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
 
     uint32_t stage = 0, phase = 0;
     int64_t f = lo;
-    RowState<D> st;  // bf16 cache: heads on the MMA's M
-    HeadState<NTH> hs;  // FP8 cache: heads on the MMA's N (fp8_block.cuh)
+    HeadState<NTH> hs;
     while (f < hi) {
         const int v = find_item(pre, V, f);
         const int s = v / a.head_tiles;
@@ -378,90 +380,53 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
         const int64_t qrow = a.query_start_loc ? a.query_start_loc[s] : s;
         const int kvh = ht * HT + hh;
         const int rows_valid = min(16, group - r0);  // query heads this warp owns
+        const __nv_bfloat16 *qw = a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
 
-        // Q fragments (A operand, rows = query heads of the group).
-        uint32_t qa[KSTEPS][4];
-        if constexpr (FP8) {
-            load_q_fp8order(qa, a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D, rows_valid, lane);
-        } else {
-            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
-                a.q + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D);
-            const bool v0 = g_row < rows_valid, v1 = g_row + 8 < rows_valid;
-#pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                const int col = ks * 16 + 2 * q4;
-                qa[ks][0] = v0 ? __ldg(q0 + (g_row * D + col) / 2) : 0u;
-                qa[ks][1] = v1 ? __ldg(q0 + ((g_row + 8) * D + col) / 2) : 0u;
-                qa[ks][2] = v0 ? __ldg(q0 + (g_row * D + col + 8) / 2) : 0u;
-                qa[ks][3] = v1 ? __ldg(q0 + ((g_row + 8) * D + col + 8) / 2) : 0u;
-            }
-        }
-        if constexpr (FP8) hs.reset();
-        else st.reset();
+        // Q fragments: the FP8 form's A operand in its k numbering, or Q^T as the B operand
+        uint32_t qa[FP8 ? KSTEPS : 1][4];
+        uint32_t qb[FP8 ? 1 : NTH][FP8 ? 1 : KSTEPS][2];
+        if constexpr (FP8) load_q_fp8order(qa, qw, rows_valid, lane);
+        else load_q_bt<D, NTH>(qb, qw, rows_valid, lane);
+        hs.reset();
 
         bool ok = true;
         for (; f < seg_end; ++f) {
             const int lb = (int)(f - item_beg);
             const int valid = min(kBS, ctx - lb * kBS);
-            // ---- S = Q K^T over the block's 16 tokens ----
+            // ---- S^T = K Q^T over the block's 16 tokens ----
             if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_ns)) { ok = false; break; }
-            float sacc[2][4];
-            if constexpr (FP8)
-                qk_block_fp8t<NTH>(reinterpret_cast<float(&)[NTH][4]>(sacc), qa,
-                                   smem_base + stage * stage_bytes + hh * (kBS * 128), lane);
-            else qk_block<D>(sacc, qa, smem_base + stage * stage_bytes + hh * (kBS * 128), chunk_stride, lane);
+            float sacc[NTH][4];
+            const uint32_t ktile = smem_base + stage * stage_bytes + hh * (kBS * 128);
+            if constexpr (FP8) qk_block_fp8t<NTH>(sacc, qa, ktile, lane);
+            else qk_block_bt<D, NTH>(sacc, qb, ktile, chunk_stride, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
 
             // ---- scale, mask the block's tail, online softmax (base 2) ----
+            // S^T: tokens g (entries 0, 1) and g + 8 (entries 2, 3) of each n-tile
             const bool tail = valid < kBS;  // only a sequence's last block
-            if constexpr (FP8) {
-                // S^T: tokens g (entries 0, 1) and g + 8 (entries 2, 3) of each n-tile
-                const bool in0 = !tail || g_row < valid, in1 = !tail || g_row + 8 < valid;
-                uint32_t pb[NTH][2];
+            const bool in0 = !tail || g_row < valid, in1 = !tail || g_row + 8 < valid;
+            uint32_t pb[NTH][2];
 #pragma unroll
-                for (int nt = 0; nt < NTH; ++nt) {
-                    sacc[nt][0] = in0 ? sacc[nt][0] * sl2 : -INFINITY;
-                    sacc[nt][1] = in0 ? sacc[nt][1] * sl2 : -INFINITY;
-                    sacc[nt][2] = in1 ? sacc[nt][2] * sl2 : -INFINITY;
-                    sacc[nt][3] = in1 ? sacc[nt][3] * sl2 : -INFINITY;
-                    softmax_update_t(hs, nt, sacc[nt], pb[nt]);
-                }
-                // ---- O^T += V^T P^T ----
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_ns)) { ok = false; break; }
-                const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-                if (tail) pv_block_fp8t<true>(hs, pb, vtile, valid, lane);
-                else pv_block_fp8t<false>(hs, pb, vtile, valid, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
-                continue;
+            for (int nt = 0; nt < NTH; ++nt) {
+                sacc[nt][0] = in0 ? sacc[nt][0] * sl2 : -INFINITY;
+                sacc[nt][1] = in0 ? sacc[nt][1] * sl2 : -INFINITY;
+                sacc[nt][2] = in1 ? sacc[nt][2] * sl2 : -INFINITY;
+                sacc[nt][3] = in1 ? sacc[nt][3] * sl2 : -INFINITY;
+                if constexpr (FP8) softmax_update_t(hs, nt, sacc[nt], pb[nt]);
+                else softmax_update_bt(hs, nt, sacc[nt], pb[nt]);
             }
-            if (tail) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool in = nt * 8 + 2 * q4 + e < valid;
-                        sacc[nt][e] = in ? sacc[nt][e] * sl2 : -INFINITY;
-                        sacc[nt][2 + e] = in ? sacc[nt][2 + e] * sl2 : -INFINITY;
-                    }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sacc[0][i] *= sl2;
-                    sacc[1][i] *= sl2;
-                }
-            }
-            uint32_t pa[4];
-            softmax_update<D>(st, sacc, pa);
-
-            // ---- O += P V ----
+            // ---- O^T += V^T P^T ----
             if (!mbar_wait(&full[stage], phase, abort_flag, a.wait_ns)) { ok = false; break; }
             const uint32_t vtile = smem_base + stage * stage_bytes + hh * (kBS * 128);
-            if (tail) pv_block<D, true>(st, pa, vtile, chunk_stride, valid, lane);
-            else pv_block<D, false>(st, pa, vtile, chunk_stride, valid, lane);
+            if constexpr (FP8) {
+                if (tail) pv_block_fp8t<true>(hs, pb, vtile, valid, lane);
+                else pv_block_fp8t<false>(hs, pb, vtile, valid, lane);
+            } else {
+                if (tail) pv_block_bt<D, true>(hs, pb, vtile, chunk_stride, valid, lane);
+                else pv_block_bt<D, false>(hs, pb, vtile, chunk_stride, valid, lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1; }
@@ -475,20 +440,20 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
         // ---- finish this item's part ----
         const int64_t seg_beg = max64(lo, item_beg);
         const bool whole = seg_beg == item_beg && seg_end == item_end;
-        if constexpr (FP8) {
-            // lane (g, t) holds dims 16g .. 16g + 15 of heads 8nt + 2t + e: dim 16g + 2mt in
-            // o[nt][mt][e], 16g + 2mt + 1 in o[nt][mt][2 + e]; the V scale comes in here
-            finish_sums_t(hs);
-            const float vs = a.v_scale;
-            const int rows = HT * group;
-            const int row0 = hh * group + r0;  // row inside the item
-            const int slot = whole ? 0 : part_slot(c, item_beg, T, ge);
+        finish_sums_t(hs);
+        const float vs = a.v_scale;  // FP8: V elements are code x v_scale (1 for bf16)
+        const int rows = HT * group;
+        const int row0 = hh * group + r0;  // row inside the item
+        const int slot = whole ? 0 : part_slot(c, item_beg, T, ge);
 #pragma unroll
-            for (int nt = 0; nt < NTH; ++nt)
+        for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int hd = 8 * nt + 2 * q4 + e;  // head inside the warp's 16
-                    if (hd >= rows_valid) continue;
+            for (int e = 0; e < 2; ++e) {
+                const int hd = 8 * nt + 2 * q4 + e;  // head inside the warp's 16
+                if (hd >= rows_valid) continue;
+                if constexpr (FP8) {
+                    // lane (g, t) holds dims 16g .. 16g + 15: dim 16g + 2mt in o[nt][mt][e],
+                    // 16g + 2mt + 1 in o[nt][mt][2 + e]
                     if (whole) {
                         const float inv = vs / hs.l[nt][e];
                         uint32_t p[8];
@@ -506,46 +471,29 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
                         for (int k = 0; k < 4; ++k)
                             ob[k] = make_float4(hs.o[nt][2 * k][e] * vs, hs.o[nt][2 * k][2 + e] * vs,
                                                 hs.o[nt][2 * k + 1][e] * vs, hs.o[nt][2 * k + 1][2 + e] * vs);
-                        if (g_row == 0)
-                            a.ws_ml[(int64_t)slot * rows + row0 + hd] = make_float2(hs.m[nt][e], hs.l[nt][e]);
+                    }
+                } else {
+                    // lane (g, t) holds dims 16mt + g (o[nt][mt][e]) and 16mt + g + 8 (o[nt][mt][2 + e])
+                    if (whole) {
+                        const float inv = 1.f / hs.l[nt][e];
+                        __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0 + hd) * D;
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            orow[16 * mt + g_row] = __float2bfloat16_rn(hs.o[nt][mt][e] * inv);
+                            orow[16 * mt + g_row + 8] = __float2bfloat16_rn(hs.o[nt][mt][2 + e] * inv);
+                        }
+                    } else {
+                        float *ob = a.ws_o + ((int64_t)slot * rows + row0 + hd) * D;
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            ob[16 * mt + g_row] = hs.o[nt][mt][e];
+                            ob[16 * mt + g_row + 8] = hs.o[nt][mt][2 + e];
+                        }
                     }
                 }
-            f = seg_end;
-            continue;
-        }
-        finish_sums<D>(st);
-        if (whole) {
-            const float inv0 = 1.f / st.l0, inv1 = 1.f / st.l1;
-            __nv_bfloat16 *orow = a.out + (qrow * a.num_heads + (int64_t)kvh * group + r0) * D;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (g_row < rows_valid)
-                    *reinterpret_cast<uint32_t *>(orow + g_row * D + col) =
-                        pack_bf16x2(st.o[n][0] * inv0, st.o[n][1] * inv0);
-                if (g_row + 8 < rows_valid)
-                    *reinterpret_cast<uint32_t *>(orow + (g_row + 8) * D + col) =
-                        pack_bf16x2(st.o[n][2] * inv1, st.o[n][3] * inv1);
+                if (!whole && g_row == 0)
+                    a.ws_ml[(int64_t)slot * rows + row0 + hd] = make_float2(hs.m[nt][e], hs.l[nt][e]);
             }
-        } else {
-            const int slot = part_slot(c, item_beg, T, ge);
-            const int rows = HT * group;
-            const int row0 = hh * group + r0;  // row inside the item
-            float *ob = a.ws_o + ((int64_t)slot * rows + row0) * D;
-            float2 *mlb = a.ws_ml + (int64_t)slot * rows + row0;
-#pragma unroll
-            for (int n = 0; n < NT_D; ++n) {
-                const int col = n * 8 + 2 * q4;
-                if (g_row < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + g_row * D + col) = make_float2(st.o[n][0], st.o[n][1]);
-                if (g_row + 8 < rows_valid)
-                    *reinterpret_cast<float2 *>(ob + (g_row + 8) * D + col) = make_float2(st.o[n][2], st.o[n][3]);
-            }
-            if (q4 == 0) {
-                if (g_row < rows_valid) mlb[g_row] = make_float2(st.m0, st.l0);
-                if (g_row + 8 < rows_valid) mlb[g_row + 8] = make_float2(st.m1, st.l1);
-            }
-        }
         f = seg_end;
     }
 }

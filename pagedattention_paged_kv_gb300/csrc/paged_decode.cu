@@ -14,7 +14,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
 template __global__ void paged_decode_kernel<64, false, 1>(const __grid_constant__ CUtensorMap,
                                                         const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<64, false, 2>(const __grid_constant__ CUtensorMap,
+                                                        const __grid_constant__ CUtensorMap, const DecodeArgs);
 template __global__ void paged_decode_kernel<128, false, 1>(const __grid_constant__ CUtensorMap,
+                                                         const __grid_constant__ CUtensorMap, const DecodeArgs);
+template __global__ void paged_decode_kernel<128, false, 2>(const __grid_constant__ CUtensorMap,
                                                          const __grid_constant__ CUtensorMap, const DecodeArgs);
 template __global__ void paged_decode_kernel<128, true, 1>(const __grid_constant__ CUtensorMap,
                                                            const __grid_constant__ CUtensorMap, const DecodeArgs);
@@ -51,10 +55,15 @@ static cudaError_t launch_decode_d(const CUtensorMap &k_map, const CUtensorMap &
 cudaError_t launch_paged_decode(int head_dim, bool fp8, const CUtensorMap &k_map, const CUtensorMap &v_map,
                                 const DecodeArgs &a, size_t smem, cudaStream_t stream) {
     if (fp8 && head_dim != 128) return cudaErrorInvalidValue;
-    if (fp8) return a.group <= 8 ? launch_decode_d<128, true, 1>(k_map, v_map, a, smem, stream)
-                                 : launch_decode_d<128, true, 2>(k_map, v_map, a, smem, stream);
-    return head_dim == 128 ? launch_decode_d<128, false, 1>(k_map, v_map, a, smem, stream)
-                           : launch_decode_d<64, false, 1>(k_map, v_map, a, smem, stream);
+    // NTH: n-tiles of 8 query heads per consumer warp
+    const bool two = a.group > 8;
+    if (fp8) return two ? launch_decode_d<128, true, 2>(k_map, v_map, a, smem, stream)
+                        : launch_decode_d<128, true, 1>(k_map, v_map, a, smem, stream);
+    if (head_dim == 128)
+        return two ? launch_decode_d<128, false, 2>(k_map, v_map, a, smem, stream)
+                   : launch_decode_d<128, false, 1>(k_map, v_map, a, smem, stream);
+    return two ? launch_decode_d<64, false, 2>(k_map, v_map, a, smem, stream)
+               : launch_decode_d<64, false, 1>(k_map, v_map, a, smem, stream);
 }
 
 }  // namespace pkv
