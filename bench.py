@@ -245,12 +245,13 @@ def kernel_source_sha(files):
 
 
 DECODE_SOURCES = ("api.cu", "paged_decode.cu", "paged_decode.cuh", "decode_cta.cuh", "attn_block.cuh",
-                  "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
+                  "bf16t_block.cuh", "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
 
 
 VARLEN_SOURCES = ("api.cu", "paged_varlen.cu", "paged_varlen.cuh", "prefill_cta.cuh", "paged_prefill.cu",
                   "paged_prefill.cuh", "decode_cta.cuh", "paged_decode.cuh", "tcgen05.cuh", "fp32x2.cuh",
-                  "attn_block.cuh", "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh", "pkv_split.cuh", "merge.cuh")
+                  "attn_block.cuh", "bf16t_block.cuh", "fp8_block.cuh", "kv_quant.cuh", "pkv_common.cuh",
+                  "pkv_split.cuh", "merge.cuh")
 
 
 def recorded_traffic(name, sources, config):
