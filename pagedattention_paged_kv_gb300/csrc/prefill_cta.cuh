@@ -17,9 +17,9 @@
 //    every K/V chunk in shared memory, so a key is read from L2 once per 256 query rows.
 //  * Keys go in 128-key chunks (8 blocks).  One elected thread issues S = Q K^T
 //    (128 x 128 x head_dim, A and B from 128-byte-swizzled shared memory) into TMEM, the
-//    half's softmax warpgroup (one thread per row) reads the row's 128 scores in one
-//    TMEM round trip, writes the bf16 weights P back over S, and O += P V runs with P as
-//    the A operand straight from TMEM.  The halves alternate on the tensor pipe, so one
+//    half's softmax warpgroup (one thread per row) reads the row's 128 scores once (two
+//    64-column TMEM loads that also return their maximum), writes the bf16 weights P
+//    back over S, and O += P V runs with P as the A operand straight from TMEM.  The halves alternate on the tensor pipe, so one
 //    half's MMAs overlap the other half's softmax.  Online softmax in base 2, rescaled
 //    only when a row's maximum grows by more than 2^8 (O is then rescaled in TMEM).
 //  * The units are (tile, 16-token key block) pairs; causal tiles stop at the block
@@ -676,67 +676,60 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &q_map, const CUte
                 // visible keys of this chunk for this row: [0, vis)
                 const int vis = (int)max64(0, min64(lim - key0, (int64_t)nkeys));
                 const bool full = __all_sync(0xffffffffu, vis >= L::KT);
-                // Two passes over the row's 128 scores, 64 columns (two loads behind one
-                // wait) at a time: a TMEM round trip costs tens of cycles, while holding all
-                // 128 scores in registers made the compiler spill the loop state.
-                auto load64 = [&](int r, uint32_t (&v)[64]) {
-                    tmem_ld32(tS + r * 64, reinterpret_cast<uint32_t(&)[32]>(v[0]));
-                    tmem_ld32(tS + r * 64 + 32, reinterpret_cast<uint32_t(&)[32]>(v[32]));
+                // One pass over the row's 128 scores in two rounds of 64 columns.  A round's
+                // loads also return its maximum (tcgen05.ld.red); the weights are taken
+                // against the row's reference maximum m_ref, which moves (lazy rescale) only
+                // when a round's maximum exceeds it by more than kRescaleSlack.  A move in the
+                // second round rescales the first round's weights, already in TMEM, and any
+                // move rescales O (both after the weights, when the scores' registers are free).
+                // A chunk with keys a row may not see (causal diagonal, context end) masks
+                // them before an ALU maximum instead.
+                float a_o = 1.f, a_p0 = 1.f;   // this chunk's scale of O / of round 0's weights
+                bool any_o = false, any_p0 = false;
+                uint64_t ps2[2] = {0, 0};
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+#pragma unroll 1
+                for (int r = 0; r < L::KT / 64; ++r) {
+                    uint32_t v[64];
+                    float red0, red1;
+                    tmem_ld32_max(tS + r * 64, reinterpret_cast<uint32_t(&)[32]>(v[0]), red0);
+                    tmem_ld32_max(tS + r * 64 + 32, reinterpret_cast<uint32_t(&)[32]>(v[32]), red1);
                     tmem_wait_ld();
                     reg_order32(reinterpret_cast<uint32_t(&)[32]>(v[0]));
                     reg_order32(reinterpret_cast<uint32_t(&)[32]>(v[32]));
+                    float rm = fmaxf(red0, red1);
                     if (!full) {
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                         for (int j = 0; j < 64; ++j)
                             if (r * 64 + j >= vis) v[j] = __float_as_uint(-INFINITY);
+#pragma unroll
+                        for (int j = 0; j < 64; j += 8)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                m4[k] = fmax3(m4[k], __uint_as_float(v[j + 2 * k]), __uint_as_float(v[j + 2 * k + 1]));
+                        rm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                     }
-                };
-                // row maximum of the raw scores (scale > 0 keeps the order)
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int r = 0; r < L::KT / 64; ++r) {
-                    uint32_t v[64];
-                    load64(r, v);
-#pragma unroll
-                    for (int j = 0; j < 64; j += 8)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            m4[k] = fmax3(m4[k], __uint_as_float(v[j + 2 * k]), __uint_as_float(v[j + 2 * k + 1]));
-                }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;  // -inf stays
-                const bool up = mx > m_ref + kRescaleSlack;
-                if (__any_sync(0xffffffffu, up)) {
-                    const float alpha = up ? fast_exp2(m_ref - mx) : 1.f;
-                    if (ch > 0) {
-                        // O holds this segment's earlier chunks (PV(c-1) is complete: the
-                        // commit behind this chunk's QK covers it); rescale it.
-                        const uint32_t gp = gh - 1;
-                        if (!mbar_wait(&pv_done[h], gp & 1, abort_flag, a.wait_ns)) { ok = false; break; }
-                        tc_fence_after();
-#pragma unroll
-                        for (int q = 0; q < D / 32; ++q) {
-                            uint32_t r[32];
-                            tmem_ld32(tO + q * 32, r);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                            tmem_st32(tO + q * 32, r);
+                    const float mx = rm * sl2;  // scale > 0 keeps the order; -inf stays
+                    const bool up = mx > m_ref + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, up)) {
+                        const float alpha = up ? fast_exp2(m_ref - mx) : 1.f;
+                        l *= alpha;
+                        ps2[0] = f2_mul(ps2[0], f2_pack(alpha, alpha));
+                        ps2[1] = f2_mul(ps2[1], f2_pack(alpha, alpha));
+                        a_o *= alpha;
+                        any_o = true;
+                        if (r > 0) {
+                            a_p0 = alpha;
+                            any_p0 = true;
                         }
-                        tmem_wait_st();
+                        if (up) m_ref = mx;
                     }
-                    l *= alpha;
-                    if (up) m_ref = mx;
-                }
-                const float base = m_ref == -INFINITY ? 0.f : m_ref;
-                // weights, written back over S as bf16 pairs: columns [16q, 16q+16) hold keys
-                // [32q, 32q+32), so a round only overwrites columns it has already read; the
-                // row sum adds the fp32 weights, two lanes at a time
-                const uint64_t sc2 = f2_pack(sl2, sl2), nb2 = f2_pack(-base, -base);
-                uint64_t ps2[2] = {0, 0};
-#pragma unroll 1
-                for (int r = 0; r < L::KT / 64; ++r) {
-                    uint32_t v[64];
-                    load64(r, v);
+                    const float base = m_ref == -INFINITY ? 0.f : m_ref;
+                    // weights, written back over S as bf16 (FP8: fp16) pairs: columns
+                    // [16q, 16q+16) hold keys [32q, 32q+32), so a round only overwrites columns
+                    // it has already read; the row sum adds the fp32 weights, two lanes at a time
+                    const uint64_t nb2 = f2_pack(-base, -base);
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         uint32_t pk[16];
@@ -759,6 +752,47 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &q_map, const CUte
                     f2_unpack(ps2[0], a0, a1);
                     f2_unpack(ps2[1], b0, b1);
                     l += (a0 + a1) + (b0 + b1);
+                }
+                if (any_p0) {
+                    // round 0's weights were taken against the reference before its move
+                    tmem_wait_st();
+#pragma unroll 1
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t w[16];
+                        tmem_ld16(tS + q * 16, w);
+                        tmem_wait_ld();
+                        reg_order16(w);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            float lo, hi;
+                            if constexpr (FP8) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+                                lo = f.x;
+                                hi = f.y;
+                            } else {
+                                lo = bf16_lo(w[j]);
+                                hi = bf16_hi(w[j]);
+                            }
+                            w[j] = FP8 ? pack_f16x2(lo * a_p0, hi * a_p0) : pack_bf16x2(lo * a_p0, hi * a_p0);
+                        }
+                        tmem_st16(tS + q * 16, w);
+                    }
+                }
+                if (any_o && ch > 0) {
+                    // O holds this segment's earlier chunks (PV(c-1) is complete: the commit
+                    // behind this chunk's QK covers it); rescale it.
+                    const uint32_t gp = gh - 1;
+                    if (!mbar_wait(&pv_done[h], gp & 1, abort_flag, a.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + q * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * a_o);
+                        tmem_st32(tO + q * 32, r);
+                    }
                 }
                 tmem_wait_st();
                 if (!FP8 && h == 0 && key0 + nkeys > ctx) {

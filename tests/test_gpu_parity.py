@@ -149,6 +149,24 @@ def test_prefill_score_jumps(factor, fp8):
         _check_step(b)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_prefill_growing_scores(fp8):
+    # K rows scaled by 1 + pos / 40: each row's scores climb along the context, so its
+    # reference maximum moves again and again, in either 64-key round of a 128-key chunk
+    # (a move in the second round rescales the first round's weights in place).
+    b = W.make_batch("growing", context_lens=[2000, 900, 40], q_lens=[64, 1, 40], num_heads=64,
+                     num_kv_heads=8, head_dim=128, seed=93, varlen=True)
+    for seq, ctx in ((0, 2000), (2, 40)):
+        for pos in range(ctx):
+            blk, off = b.block_tables[seq, pos // b.block_size], pos % b.block_size
+            b.k_cache[blk, off] = W.bf16_bits(W.bf16_to_f32(b.k_cache[blk, off]) * np.float32(1 + pos / 40))
+    if fp8:
+        from test_gpu_fp8 import _check_fp8
+        _check_fp8(W.to_fp8_pool(b, k_scale=1.0))  # |K| stays below ~300, inside e4m3's range
+    else:
+        _check_step(b)
+
+
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 64), (8, 2, 128), (12, 4, 64), (56, 8, 128)])
 def test_varlen_head_layouts(Hq, Hkv, d):
     b = W.make_batch("varlen_heads", context_lens=[70, 3, 129], q_lens=[37, 1, 129], num_heads=Hq,
