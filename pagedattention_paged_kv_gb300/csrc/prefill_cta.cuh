@@ -304,9 +304,9 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &q_map, const CUte
         mbar_init(mma_done, 1);
         for (int h = 0; h < 2; ++h) {
             mbar_init(&s_full[h], 1);
-            mbar_init(&p_full[h], 128);
+            mbar_init(&p_full[h], 4);  // one arrival per softmax warp
             mbar_init(&pv_done[h], 1);
-            mbar_init(&o_free[h], 128);
+            mbar_init(&o_free[h], 4);
         }
         for (int i = 0; i < NST; ++i) {
             mbar_init(&kv_full[i], FP8 ? 64 : 1);  // FP8: the 64 converter threads arrive
@@ -810,8 +810,10 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &q_map, const CUte
                     }
                     fence_async_smem();
                 }
+                // every lane's TMEM stores are complete (wait::st); one lane arrives for the warp
                 tc_fence_before();
-                mbar_arrive(&p_full[h]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[h]);
             }
             if (!ok) break;
             // ---- epilogue: O / l for the tile, or the part for the merge ----
@@ -893,7 +895,8 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap &q_map, const CUte
             }
             if (!whole && rvalid) a.ws_ml[(int64_t)slot * tile_rows + trow] = make_float2(m_ref, l);
             tc_fence_before();
-            mbar_arrive(&o_free[h]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[h]);
             f = sg.end;
         }
         if (!ok) {
