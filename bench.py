@@ -727,6 +727,48 @@ def main():
 
     if rank != 0:
         return
+    # The skewed workload's split-K ablation: the same attention call with every (sequence,
+    # KV-head tile) item computed whole by one CTA (no partial items, no merge work), timed
+    # the same way (graph replay, L2 flushed, events created before the loop).
+    ablation = None
+    if args.config == "skewed_decode":
+        pkv.set_decode_split(False)
+        try:
+            with torch.cuda.stream(ts):
+                for _ in range(2):
+                    attention()
+            torch.cuda.synchronize()
+            assert pkv.get_device_error() == 0
+            abl_graph = None
+            if not args.eager_step:
+                from pagedattention_paged_kv_gb300.graph import CapturedStep
+                abl_graph = CapturedStep(attention, stream=ts)
+            n_abl = min(args.steps, 50)
+            abl_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_abl)]
+            for e2 in abl_ev:
+                for e in e2:
+                    e.record(ts)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(ts):
+                for i in range(warmup + n_abl):
+                    l2_flush(i)
+                    if i >= warmup:
+                        abl_ev[i - warmup][0].record(ts)
+                    if abl_graph is not None:
+                        abl_graph.replay()
+                    else:
+                        attention()
+                    if i >= warmup:
+                        abl_ev[i - warmup][1].record(ts)
+            torch.cuda.synchronize()
+            assert pkv.get_device_error() == 0
+        finally:
+            pkv.set_decode_split(True)
+        abl_ms = [e[0].elapsed_time(e[1]) for e in abl_ev]
+        t_abl = sum(abl_ms) / len(abl_ms)
+        ablation = {"what": "split-K off: every (sequence, KV-head tile) item computed whole by one CTA, "
+                            "no merge work", "attention_us": 1e3 * t_abl, "timing": spread(abl_ms),
+                    "gb_s": attn_bytes / (t_abl * 1e-3) / 1e9, "time_vs_split": t_abl / t_attn}
     launches_per_step = (0 if fused else 1) + (2 if not varlen else pkv.attention_launches(max_q_len))
     line = {
         "metric": METRIC if args.config == "gqa_decode" else f"{name}: HBM GB/s of the step",
@@ -759,6 +801,8 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if ablation is not None:
+        line["split_ablation"] = ablation
     if varlen and args.part == "chunk":
         fl = chunk_flops(b.context_lens, b.q_lens, d, Hq)
         tf = fl / (t_attn * 1e-3) / 1e12

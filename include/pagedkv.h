@@ -310,6 +310,16 @@ int pkv_copy_to_host(void *dst, const void *src, size_t bytes, void *stream);
  */
 void pkv_set_wait_limit_ns(uint64_t limit_ns);
 
+/*
+ * Split-K of the decode rows for launches from now on (process-wide).  enabled != 0 (the
+ * default): the blocks of all (sequence, KV-head tile) items are cut into equal shares,
+ * one per CTA, and partial results are merged by log-sum-exp weights.  enabled == 0: every
+ * item is computed whole by one CTA (each share boundary moves back to the first block of
+ * the item it falls in; no merge work), the split's ablation: a long context then costs
+ * one CTA's streaming time.  Results agree within rounding.  Not from the pages.
+ */
+void pkv_set_decode_split(int enabled);
+
 /* Workspace bytes the op needs on the current device for these sizes (0 if the
  * sizes are unsupported).  Does not allocate. */
 size_t pkv_workspace_size(int op, int num_seqs, int total_q_tokens, int num_heads,

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_copy_to_host.argtypes = [vp, vp, sz, vp]
         L.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.pkv_set_wait_limit_ns.restype = None
+        L.pkv_set_decode_split.argtypes = [ctypes.c_int]
+        L.pkv_set_decode_split.restype = None
         L.pkv_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.pkv_workspace_size.restype = sz
         L.pkv_status_string.argtypes = [i32]
@@ -347,6 +349,12 @@ def set_wait_limit_ns(limit_ns: int) -> None:
     2 s).  A wait that runs out flags DEVERR_TIMEOUT and the kernel returns; short limits
     exist to test that failure path."""
     lib().pkv_set_wait_limit_ns(int(limit_ns))
+
+
+def set_decode_split(enabled: bool) -> None:
+    """Split-K of the decode rows for launches from now on (default on).  Off, every
+    (sequence, KV-head tile) item is computed whole by one CTA: the split's ablation."""
+    lib().pkv_set_decode_split(1 if enabled else 0)
 
 
 def get_device_error(stream=None) -> int:

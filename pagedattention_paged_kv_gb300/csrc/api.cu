@@ -51,6 +51,8 @@ DeviceInfo g_dev[kMaxDevices];
 
 // Limit of a kernel's pipeline waits (pkv_set_wait_limit_ns); read at each launch.
 std::atomic<uint64_t> g_wait_ns{pkv::kWaitTimeoutNs};
+// Split-K of the decode rows (pkv_set_decode_split); read at each launch.
+std::atomic<int> g_decode_split{1};
 
 // Measured GB300 rates behind the varlen grid split (paged_varlen.cu).  A decode CTA that
 // shares the GPU with prefill CTAs streams ~83 GB/s of bf16 K/V (~42 GB/s of FP8 codes);
@@ -254,6 +256,7 @@ int prepare_decode(pkv::DecodeArgs &a, CUtensorMap &kmap, CUtensorMap &vmap, voi
     a.ws_o = reinterpret_cast<float *>(ws + p.off_o);
     a.err = d.err;
     a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.whole_items = g_decode_split.load(std::memory_order_relaxed) ? 0 : 1;
     return PKV_OK;
 }
 
@@ -306,6 +309,10 @@ extern "C" int pkv_get_device_error(void *stream) {
     if (cudaMemsetAsync(d->err, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
     return h;
+}
+
+extern "C" void pkv_set_decode_split(int enabled) {
+    g_decode_split.store(enabled ? 1 : 0, std::memory_order_relaxed);
 }
 
 extern "C" void pkv_set_wait_limit_ns(uint64_t limit_ns) {

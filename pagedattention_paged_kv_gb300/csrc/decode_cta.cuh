@@ -113,6 +113,12 @@ __device__ __forceinline__ int find_item(const int32_t *pre, int V, int64_t f) {
     return lo;
 }
 
+// Unit f moved back to the first unit of its item (T stays T): with every share boundary
+// moved so, each item lies whole in the share holding its first unit.
+__device__ __forceinline__ int64_t item_floor(const int32_t *pre, int V, int64_t T, int64_t f) {
+    return f >= T ? T : (int64_t)pre[find_item(pre, V, f)];
+}
+
 }  // namespace
 
 // CTA 0: one merge job per boundary between CTA shares (the item split there, when that
@@ -124,7 +130,7 @@ __device__ void write_jobs_and_empty_rows(const DecodeArgs &a, const int32_t *pr
     for (int b = threadIdx.x; b < a.grid; b += blockDim.x) {
         MergeJob j;
         no_job(j);
-        if (T > 0 && b < ge - 1) {
+        if (T > 0 && b < ge - 1 && !a.whole_items) {
             const int64_t f = share_begin(b + 1, T, ge);
             const int v = find_item(pre, V, f);
             const int64_t item_beg = pre[v];
@@ -212,7 +218,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &k_map, const CUten
     if (cta == 0) write_jobs_and_empty_rows<D>(a, pre, V, T, ge);
     if (cta >= ge || T == 0) return;
     const int c = cta;
-    const int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
+    int64_t lo = share_begin(c, T, ge), hi = share_begin(c + 1, T, ge);
+    if (a.whole_items) {  // the split-K ablation: no partial items, no merge jobs
+        lo = item_floor(pre, V, T, lo);
+        hi = item_floor(pre, V, T, hi);
+    }
 
     if (warp == ncw) {
         // ------------------------------ producer ------------------------------

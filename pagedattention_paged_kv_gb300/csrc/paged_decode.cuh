@@ -27,6 +27,7 @@ struct DecodeArgs {
     int num_stages;      // shared-memory ring depth (K and V of a block take one stage each)
     int grid;            // CTAs launched
     int min_blocks_per_cta;
+    int whole_items;     // 1: no item is split across CTAs (shares end at item boundaries)
     int64_t num_blocks;
     float scale_log2;    // scale * log2(e) (times the K scale for an FP8 cache)
     float v_scale;       // FP8 cache: V element = code value * v_scale (1 otherwise)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import compare, gpu_step, oracle_step
+import pagedattention_paged_kv_gb300 as pkv
 from pagedattention_paged_kv_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -147,6 +148,25 @@ def test_prefill_score_jumps(factor, fp8):
         _check_fp8(W.to_fp8_pool(b, k_scale=1.0))
     else:
         _check_step(b)
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_decode_split_off_computes_items_whole(varlen):
+    # The split-K ablation: with the split off every (sequence, KV-head tile) item is
+    # computed whole by one CTA and no merge job runs; results stay within tolerance.
+    # Short contexts and two long ones (one item then spans several CTA shares); the varlen
+    # form adds a prefill chunk, so the decode CTAs of the one-launch kernel take the mode.
+    ctx = [300, 17, 1200, 5000, 64, 9000, 700, 1]
+    ql = [1] * len(ctx)
+    if varlen:
+        ctx, ql = ctx + [400], ql + [100]
+    b = W.make_batch("split_off", context_lens=ctx, q_lens=ql, num_heads=64, num_kv_heads=8,
+                     head_dim=128, seed=95, varlen=varlen, pool_fill="nan")
+    pkv.set_decode_split(False)
+    try:
+        _check_step(b)
+    finally:
+        pkv.set_decode_split(True)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
