@@ -71,6 +71,8 @@ def parse():
     p.add_argument("--part", choices=["all", "chunk", "decodes"], default="all",
                    help="varlen workloads: time the step on its prefill chunks only or its decode rows "
                         "only (the same batch restricted to those sequences)")
+    p.add_argument("--no-split", action="store_true",
+                   help="decode rows without the split-K: every (sequence, KV-head tile) item whole in one CTA")
     p.add_argument("--separate-kv-write", action="store_true",
                    help="decode workloads: run the KV write as its own launch instead of fused into decode")
     return p.parse_args()
@@ -506,6 +508,9 @@ def main():
         ql = b.q_lens
         b = W.select_seqs(b, np.nonzero(ql >= 2 if args.part == "chunk" else ql == 1)[0])
         name = f"{name} ({args.part} only)"
+    if args.no_split:
+        pkv.set_decode_split(False)
+        name = f"{name} (split-K off)"
     varlen = b.query_start_loc is not None
     total_bytes, attn_bytes = algorithmic_bytes(b)
     S, Hq, d = b.num_seqs, b.num_heads, b.head_dim
