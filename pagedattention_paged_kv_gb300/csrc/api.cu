@@ -241,7 +241,7 @@ int prepare_decode(pkv::DecodeArgs &a, CUtensorMap &kmap, CUtensorMap &vmap, voi
     a.warps_per_head = p.warps_per_head;
     a.num_stages = p.num_stages;
     a.grid = p.grid;
-    a.min_blocks_per_cta = 8;
+    a.min_blocks_per_cta = 2;
     a.num_blocks = num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f * k_scale;
     a.v_scale = v_scale;
